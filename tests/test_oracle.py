@@ -1,0 +1,438 @@
+"""Pins for the float64 oracle: what the pages and the mathematics fix.
+
+Every check here is independent of the oracle's own formulas: the worked
+example of the Flash Attention 2 post (transcribed under tests/golden/),
+closed forms, invariants stated on the pages, library routines (SciPy),
+pure-Python brute force, and central finite differences. The last block
+plants mistakes in the oracle and checks that these pins catch them.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import oracle.attention as oa
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "fa2_worked_example.txt")
+
+
+# ---------------------------------------------------------------- helpers
+
+def _parse_golden(path):
+    out = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, val = (x.strip() for x in line.split("=", 1))
+            out[key] = val
+    return out
+
+
+def _closed(term_list):
+    """'c@e c@e ...' -> sum(c * e^e), evaluated in float64."""
+    total = 0.0
+    for t in term_list.split():
+        c, e = t.split("@")
+        total += float(c) * math.exp(float(e))
+    return total
+
+
+def _matrix(val):
+    return np.array([[float(x) for x in row.split()] for row in val.split(";")])
+
+
+def _closed_vector(val):
+    return np.array([_closed(row) for row in val.split(";")])
+
+
+def _closed_matrix(val):
+    return np.array([[_closed(e) for e in row.split("|")] for row in val.split(";")])
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def _brute_attention(q, k, v, scale, causal):
+    """Pure-Python loops over one head: the definition, entry by entry."""
+    nq, nk, dv = len(q), len(k), len(v[0])
+    out, lse = [], []
+    for i in range(nq):
+        s = []
+        for j in range(nk):
+            if causal and j > i + (nk - nq):
+                continue
+            s.append((j, scale * sum(q[i][t] * k[j][t] for t in range(len(q[i])))))
+        if not s:
+            out.append([0.0] * dv)
+            lse.append(-math.inf)
+            continue
+        mx = max(x for _, x in s)
+        z = sum(math.exp(x - mx) for _, x in s)
+        row = [sum(math.exp(x - mx) / z * v[j][c] for j, x in s) for c in range(dv)]
+        out.append(row)
+        lse.append(mx + math.log(z))
+    return np.array(out), np.array(lse)
+
+
+# ------------------------------------------------ worked example (golden)
+
+def test_worked_example_inner_steps():
+    g = _parse_golden(GOLDEN)
+    q, kt, v = _matrix(g["Q"]), _matrix(g["KT"]), _matrix(g["V"])
+    states = {}
+    oracle.tiled_forward(q, kt.T, v, 1.0, 2, 2,
+                         trace=lambda i, j, st: states.__setitem__((i, j), st))
+    for j in range(3):
+        st = states[(0, j)]
+        tag = f"1_{j + 1}"
+        np.testing.assert_array_equal(st["S"], _matrix(g[f"S_{tag}"]))
+        np.testing.assert_array_equal(st["m_ij"], _matrix(g[f"m_local_{tag}"])[0])
+        np.testing.assert_array_equal(st["m"], _matrix(g[f"m_run_{tag}"])[0])
+        np.testing.assert_allclose(st["l"], _closed_vector(g[f"l_run_{tag}"]), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(st["O"], _closed_matrix(g[f"O_run_{tag}"]), rtol=0, atol=1e-14)
+
+
+def test_worked_example_printed_decimals():
+    g = _parse_golden(GOLDEN)
+    q, kt, v = _matrix(g["Q"]), _matrix(g["KT"]), _matrix(g["V"])
+    states = {}
+    oracle.tiled_forward(q, kt.T, v, 1.0, 2, 2,
+                         trace=lambda i, j, st: states.__setitem__((i, j), st))
+    st = states[(0, 2)]
+    np.testing.assert_allclose(st["l"], _matrix(g["l_run_1_3_printed"])[0], atol=5e-5)
+    printed = _matrix(g["O_run_1_3_printed"])
+    # Three printed entries agree to their 3 decimals; the [0,0] entry is the
+    # page's slip (closed form 3.77253 vs printed 3.768).
+    mask = np.ones_like(printed, dtype=bool)
+    mask[0, 0] = False
+    np.testing.assert_allclose(st["O"][mask], printed[mask], atol=5e-4)
+    assert abs(st["O"][0, 0] - 3.772533) < 1e-6
+
+
+def test_worked_example_tiled_equals_standard():
+    g = _parse_golden(GOLDEN)
+    q, kt, v = _matrix(g["Q"]), _matrix(g["KT"]), _matrix(g["V"])
+    o_t, lse_t = oracle.tiled_forward(q, kt.T, v, 1.0, 2, 2)
+    o_s, lse_s = oracle.attention_fwd(q[None, None], kt.T[None, None], v[None, None], 1.0)
+    bound = float(g["tiled_vs_standard_max_abs"])
+    assert np.max(np.abs(o_t - o_s[0, 0])) <= 4 * bound
+    assert np.max(np.abs(lse_t - lse_s[0, 0])) <= 1e-14
+    # O_1 = Õ_1 ⊘ l_1 (Step 6) with the closed forms of the last inner step
+    o1 = _closed_matrix(g["O_run_1_3"]) / _closed_vector(g["l_run_1_3"])[:, None]
+    np.testing.assert_allclose(o_s[0, 0, :2], o1, rtol=0, atol=1e-14)
+    lse1 = _matrix(g["m_run_1_3"])[0] + np.log(_closed_vector(g["l_run_1_3"]))
+    np.testing.assert_allclose(lse_s[0, 0, :2], lse1, rtol=0, atol=1e-14)
+
+
+# -------------------------------------------------- forward invariants
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prob_rows_sum_to_one(causal):
+    q, k = _rand((37, 16), 1), _rand((37, 16), 2)
+    p = oracle.attention_probs(q, k, 0.25, causal)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+    assert (p >= 0).all()
+    if causal:
+        assert (p[np.triu_indices(37, 1)] == 0).all()
+
+
+def test_shift_invariance():
+    s = _rand((9, 23), 3, 4.0)
+    c = _rand((9, 1), 4, 30.0)
+    np.testing.assert_allclose(oracle.softmax_rows(s + c), oracle.softmax_rows(s), atol=1e-15)
+    np.testing.assert_allclose(oracle.logsumexp_rows(s + c), oracle.logsumexp_rows(s) + c[:, 0],
+                               atol=1e-12)
+
+
+def test_softmax_matches_scipy():
+    q, k = _rand((40, 32), 5), _rand((50, 32), 6)
+    s = 0.3 * q @ k.T
+    np.testing.assert_allclose(oracle.softmax_rows(s), scipy.special.softmax(s, axis=1), atol=1e-15)
+    np.testing.assert_allclose(oracle.logsumexp_rows(s), scipy.special.logsumexp(s, axis=1),
+                               atol=1e-13)
+
+
+@pytest.mark.parametrize("causal,nq,nk", [(False, 5, 7), (True, 6, 6), (True, 3, 8), (False, 1, 1)])
+def test_brute_force_tiny(causal, nq, nk):
+    q, k, v = _rand((nq, 3), 7), _rand((nk, 3), 8), _rand((nk, 2), 9)
+    o_ref, lse_ref = _brute_attention(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
+    o, lse = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 0.7, causal)
+    np.testing.assert_allclose(o[0, 0], o_ref, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], lse_ref, atol=1e-13)
+
+
+def test_identical_keys_give_mean_of_v():
+    k = np.tile(_rand((1, 8), 10), (12, 1))
+    q, v = _rand((5, 8), 11), _rand((12, 4), 12)
+    o, lse = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 0.5)
+    np.testing.assert_allclose(o[0, 0], np.tile(v.mean(axis=0), (5, 1)), atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], 0.5 * q @ k[0] + math.log(12), atol=1e-13)
+
+
+def test_single_key():
+    q, k, v = _rand((4, 6), 13), _rand((1, 6), 14), _rand((1, 6), 15)
+    o, lse = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 0.9)
+    np.testing.assert_allclose(o[0, 0], np.tile(v[0], (4, 1)), atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0], 0.9 * q @ k[0], atol=1e-14)
+
+
+def test_causal_first_row_and_offsets():
+    q, k, v = _rand((6, 4), 16), _rand((6, 4), 17), _rand((6, 4), 18)
+    o, lse = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 1.0, True)
+    np.testing.assert_allclose(o[0, 0, 0], v[0], atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0, 0], q[0] @ k[0], atol=1e-14)
+    # bottom-right alignment: the last query row sees every key
+    o_full, _ = oracle.attention_fwd(q[None, None, -1:], k[None, None], v[None, None], 1.0, False)
+    np.testing.assert_allclose(o[0, 0, -1], o_full[0, 0, 0], atol=1e-15)
+
+
+def test_large_scale_selects_argmax():
+    q, k, v = _rand((7, 16), 19), _rand((11, 16), 20), _rand((11, 3), 21)
+    o, _ = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 200.0)
+    np.testing.assert_allclose(o[0, 0], v[np.argmax(q @ k.T, axis=1)], atol=1e-6)
+
+
+def test_gqa_equals_repeated_heads():
+    B, Hq, Hkv, N, d = 2, 6, 2, 9, 5
+    q, k, v = _rand((B, Hq, N, d), 22), _rand((B, Hkv, N, d), 23), _rand((B, Hkv, N, d), 24)
+    o, lse = oracle.attention_fwd(q, k, v, 0.4, True)
+    r = Hq // Hkv
+    o2, lse2 = oracle.attention_fwd(q, np.repeat(k, r, axis=1), np.repeat(v, r, axis=1), 0.4, True)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_rows_subset_matches_full():
+    B, H, N, d = 1, 2, 40, 8
+    q, k, v = _rand((B, H, N, d), 25), _rand((B, H, N, d), 26), _rand((B, H, N, d), 27)
+    o, lse = oracle.attention_fwd(q, k, v, 0.3, True)
+    rows = [0, 5, 17, 39]
+    o_r, lse_r = oracle.attention_fwd_rows(q, k, v, 0.3, True, 0, 1, rows)
+    np.testing.assert_array_equal(o_r, o[0, 1, rows])
+    np.testing.assert_array_equal(lse_r, lse[0, 1, rows])
+
+
+@pytest.mark.parametrize("br,bc,nq,nk,causal", [
+    (2, 2, 6, 6, False), (3, 5, 17, 23, False), (4, 4, 16, 16, True),
+    (5, 3, 11, 19, True), (64, 64, 10, 10, False), (1, 7, 9, 30, True)])
+def test_tiled_equals_full(br, bc, nq, nk, causal):
+    q, k, v = _rand((nq, 8), 28, 2.0), _rand((nk, 8), 29, 2.0), _rand((nk, 6), 30)
+    o_t, lse_t = oracle.tiled_forward(q, k, v, 0.8, br, bc, causal)
+    o_s, lse_s = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 0.8, causal)
+    np.testing.assert_allclose(o_t, o_s[0, 0], atol=1e-13)
+    np.testing.assert_allclose(lse_t, lse_s[0, 0], atol=1e-13)
+
+
+# -------------------------------------------------- backward pins
+
+def _loss_grads_fd(q, k, v, g, scale, causal, h=1e-6):
+    """Central differences of L = Σ g ∘ O(q, k, v) for every input entry."""
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention_fwd(q_, k_, v_, scale, causal)
+        return float((g * o).sum())
+    grads = []
+    for which in range(3):
+        xs = [q.copy(), k.copy(), v.copy()]
+        x = xs[which]
+        gr = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            x0 = x[idx]
+            x[idx] = x0 + h
+            lp = loss(*xs)
+            x[idx] = x0 - h
+            lm = loss(*xs)
+            x[idx] = x0
+            gr[idx] = (lp - lm) / (2 * h)
+        grads.append(gr)
+    return grads
+
+
+def _fd_error(causal, hq=2, hkv=1, n=6, d=4, route="jvp"):
+    rng_seed = 31 + hq + n + int(causal)
+    q = _rand((1, hq, n, d), rng_seed)
+    k = _rand((1, hkv, n, d), rng_seed + 1)
+    v = _rand((1, hkv, n, d), rng_seed + 2)
+    g = _rand((1, hq, n, d), rng_seed + 3)
+    an = oracle.attention_bwd(q, k, v, g, 0.6, causal, route=route)
+    fd = _loss_grads_fd(q, k, v, g, 0.6, causal)
+    return max(np.max(np.abs(a - f)) for a, f in zip(an, fd))
+
+
+@pytest.mark.parametrize("causal,hq,hkv,n", [(False, 1, 1, 5), (True, 2, 2, 7), (True, 4, 2, 6),
+                                             (False, 3, 1, 4)])
+def test_bwd_finite_differences(causal, hq, hkv, n):
+    assert _fd_error(causal, hq, hkv, n) < 1e-7
+
+
+def test_bwd_jacobian_route_equals_jvp_route():
+    q, k, v, do = (_rand((2, 2, 33, 8), s) for s in (40, 41, 42, 43))
+    for causal in (False, True):
+        a = oracle.attention_bwd(q, k, v, do, 0.35, causal, route="jvp")
+        b = oracle.attention_bwd(q, k, v, do, 0.35, causal, route="jacobian")
+        for x, y in zip(a, b):
+            np.testing.assert_allclose(x, y, atol=1e-12)
+
+
+def test_softmax_jacobian_symmetric_and_fd():
+    s = _rand(9, 44, 2.0)
+    p = oracle.softmax_rows(s[None])[0]
+    j = oracle.softmax_jacobian(p)
+    np.testing.assert_allclose(j, j.T, atol=0)
+    h = 1e-6
+    fd = np.stack([(oracle.softmax_rows((s + h * e)[None])[0] - oracle.softmax_rows((s - h * e)[None])[0])
+                   / (2 * h) for e in np.eye(9)], axis=1)
+    np.testing.assert_allclose(j, fd, atol=1e-9)
+
+
+def test_softmax_backward_rows_sum_to_zero():
+    p = oracle.softmax_rows(_rand((12, 20), 45, 3.0))
+    ds = oracle.softmax_backward_jvp(p, _rand((12, 20), 46))
+    np.testing.assert_allclose(ds.sum(axis=1), 0.0, atol=1e-15)
+
+
+def test_row_term_two_ways():
+    """rowsum(P ∘ dP) = rowsum(dO ∘ O): the row term the GPU computes from O."""
+    q, k, v, do = (_rand((30, 8), s) for s in (47, 48, 49, 50))
+    for causal in (False, True):
+        p = oracle.attention_probs(q, k, 0.5, causal)
+        o = p @ v
+        dp = do @ v.T
+        np.testing.assert_allclose((p * dp).sum(axis=1), (do * o).sum(axis=1), atol=1e-13)
+
+
+def test_gqa_backward_sums_group():
+    B, Hq, Hkv, N, d = 1, 4, 2, 7, 3
+    q, do = _rand((B, Hq, N, d), 51), _rand((B, Hq, N, d), 52)
+    k, v = _rand((B, Hkv, N, d), 53), _rand((B, Hkv, N, d), 54)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.5, True)
+    r = Hq // Hkv
+    dq2, dk2, dv2 = oracle.attention_bwd(q, np.repeat(k, r, 1), np.repeat(v, r, 1), do, 0.5, True)
+    np.testing.assert_allclose(dq, dq2, atol=1e-14)
+    np.testing.assert_allclose(dk, dk2.reshape(B, Hkv, r, N, d).sum(2), atol=1e-14)
+    np.testing.assert_allclose(dv, dv2.reshape(B, Hkv, r, N, d).sum(2), atol=1e-14)
+
+
+# -------------------------------------------------- decode / merge pins
+
+def _decode_inputs(B=2, Hq=4, Hkv=2, L=37, d=8, seed=60):
+    return _rand((B, Hq, d), seed), _rand((B, Hkv, L, d), seed + 1), _rand((B, Hkv, L, d), seed + 2)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16, 37, 50])
+def test_decode_split_equals_attention(splits):
+    q, k, v = _decode_inputs()
+    o, lse = oracle.decode_splitkv(q, k, v, 0.3, splits)
+    o_ref, lse_ref = oracle.attention_fwd(q[:, :, None], k, v, 0.3)
+    np.testing.assert_allclose(o, o_ref[:, :, 0], atol=1e-14)
+    np.testing.assert_allclose(lse, lse_ref[:, :, 0], atol=1e-13)
+
+
+def test_decode_partials_closed_form():
+    q, k, v = _decode_inputs(B=1, Hq=1, Hkv=1, L=6, d=3)
+    o_p, m_p, l_p = oracle.decode_split_partials(q, k, v, 1.0, 2)
+    for s in range(2):
+        sc = [sum(q[0, 0, t] * k[0, 0, j, t] for t in range(3)) for j in range(3 * s, 3 * s + 3)]
+        mx = max(sc)
+        assert m_p[0, 0, s] == pytest.approx(mx, abs=1e-14)
+        assert l_p[0, 0, s] == pytest.approx(sum(math.exp(x - mx) for x in sc), abs=1e-14)
+        want = [sum(math.exp(x - mx) * v[0, 0, 3 * s + j, c] for j, x in enumerate(sc)) for c in range(3)]
+        np.testing.assert_allclose(o_p[0, 0, s], want, atol=1e-14)
+
+
+def test_merge_order_independent_and_empty_split():
+    q, k, v = _decode_inputs()
+    o_p, m_p, l_p = oracle.decode_split_partials(q, k, v, 0.3, 8)
+    o1, lse1 = oracle.merge_partials(o_p, m_p, l_p)
+    perm = np.random.default_rng(0).permutation(8)
+    o2, lse2 = oracle.merge_partials(o_p[:, :, perm], m_p[:, :, perm], l_p[:, :, perm])
+    np.testing.assert_allclose(o1, o2, atol=1e-14)
+    np.testing.assert_allclose(lse1, lse2, atol=1e-13)
+    # appending empty splits (m=-inf, l=0, o=0) leaves the result unchanged
+    pad = lambda x, val: np.concatenate([x, np.full(x.shape[:2] + (3,) + x.shape[3:], val)], axis=2)
+    o3, lse3 = oracle.merge_partials(pad(o_p, 0.0), pad(m_p, -np.inf), pad(l_p, 0.0))
+    np.testing.assert_allclose(o3, o1, atol=1e-15)
+    np.testing.assert_allclose(lse3, lse1, atol=1e-15)
+    # all-empty rows: O = 0, LSE = -inf
+    o4, lse4 = oracle.merge_partials(np.zeros((1, 2, 3)), np.full((1, 2), -np.inf), np.zeros((1, 2)))
+    assert (o4 == 0).all() and np.isneginf(lse4).all()
+
+
+def test_fully_masked_row_is_zero():
+    # causal with Nq > Nk: the first rows see no key under bottom-right alignment
+    q, k, v = _rand((5, 4), 70), _rand((3, 4), 71), _rand((3, 4), 72)
+    o, lse = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 1.0, True)
+    assert (o[0, 0, :2] == 0).all() and np.isneginf(lse[0, 0, :2]).all()
+    o_t, lse_t = oracle.tiled_forward(q, k, v, 1.0, 2, 2, True)
+    np.testing.assert_allclose(o_t, o[0, 0], atol=1e-14)
+    np.testing.assert_array_equal(np.isneginf(lse_t), np.isneginf(lse[0, 0]))
+
+
+# ------------------------------------- planted mistakes must fail a pin
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Each mutant below is a plausible slip; at least one pin must fail."""
+    g = _parse_golden(GOLDEN)
+    q, kt, v = _matrix(g["Q"]), _matrix(g["KT"]), _matrix(g["V"])
+
+    def worked_example_error():
+        o_s, _ = oracle.attention_fwd(q[None, None], kt.T[None, None], v[None, None], 1.0)
+        o1 = _closed_matrix(g["O_run_1_3"]) / _closed_vector(g["l_run_1_3"])[:, None]
+        return np.max(np.abs(o_s[0, 0, :2] - o1))
+
+    def causal_brute_error():
+        qq, kk, vv = _rand((6, 3), 80), _rand((6, 3), 81), _rand((6, 2), 82)
+        o_ref, _ = _brute_attention(qq.tolist(), kk.tolist(), vv.tolist(), 1.0, True)
+        o, _ = oracle.attention_fwd(qq[None, None], kk[None, None], vv[None, None], 1.0, True)
+        return np.max(np.abs(o[0, 0] - o_ref))
+
+    def gqa_error():
+        qq, kk, vv = _rand((1, 4, 5, 3), 83), _rand((1, 2, 5, 3), 84), _rand((1, 2, 5, 3), 85)
+        o, _ = oracle.attention_fwd(qq, kk, vv, 1.0)
+        o2 = np.stack([_brute_attention(qq[0, h].tolist(), kk[0, h // 2].tolist(),
+                                        vv[0, h // 2].tolist(), 1.0, False)[0] for h in range(4)])
+        return np.max(np.abs(o[0] - o2))
+
+    def merge_error():
+        qq, kk, vv = _decode_inputs()
+        o, _ = oracle.decode_splitkv(qq, kk, vv, 0.3, 5)
+        o_ref, _ = _brute_attention([qq[0, 0].tolist()], kk[0, 0].tolist(), vv[0, 0].tolist(), 0.3, False)
+        return np.max(np.abs(o[0, 0] - o_ref[0]))
+
+    checks = [worked_example_error, causal_brute_error, gqa_error, merge_error,
+              lambda: _fd_error(True, 2, 1, 5)]
+    assert max(c() for c in checks) < 1e-7  # the real oracle passes every pin
+
+    orig_jvp = oa.softmax_backward_jvp
+    orig_allowed = oa.causal_allowed
+    orig_softmax = oa.softmax_rows
+    orig_exp_diff = oa._exp_diff
+    mutants = {
+        "dS without the row term": ("softmax_backward_jvp", lambda p, g_: p * g_),
+        "dS with a flipped sign": ("softmax_backward_jvp", lambda p, g_: -orig_jvp(p, g_)),
+        "causal mask off by one": ("causal_allowed",
+                                   lambda nq, nk, rows=None: orig_allowed(nq, nk + 1, rows)[:, :nk]),
+        "GQA grouping interleaved": ("_kv_head", lambda h, hq, hkv: h % hkv),
+        "softmax over columns": ("softmax_rows", lambda s: orig_softmax(s.T).T if s.shape[0] == s.shape[1]
+                                 else orig_softmax(s) * 0.5),
+        "merge weight inverted": ("_exp_diff", lambda a, b: orig_exp_diff(b, a) if np.ndim(a) == 3
+                                  else orig_exp_diff(a, b)),
+    }
+    for name, (attr, fn) in mutants.items():
+        with monkeypatch.context() as mp:
+            mp.setattr(oa, attr, fn)
+            errs = []
+            for c in checks:
+                try:
+                    errs.append(c())
+                except Exception:  # a crash also counts as caught
+                    errs.append(np.inf)
+            assert max(errs) > 1e-6, f"pins missed the planted mistake: {name}"

@@ -1,0 +1,89 @@
+"""Seeded synthetic workloads: shapes and input tensors.
+
+This module is shared by the tests, ``bench.py`` and ``__graft_entry__``. It
+holds only shapes, seeds and random draws: none of the attention arithmetic
+(that lives in the CUDA library and, separately, in the test oracle).
+
+Recipe: one CPU ``torch.Generator`` seeded per workload; float32 N(0, 1)
+draws in the order Q, K, V, then dO for a backward workload; each tensor is
+then cast to the workload's dtype (bf16 by round-to-nearest-even). Both the
+GPU path and the oracle see exactly these cast values.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str          # "fwd", "bwd" or "decode"
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int            # query rows per head (1 for decode)
+    Nk: int            # key rows per head (KV length for decode)
+    d: int
+    dtype: str         # "f32" or "bf16"
+    causal: bool = False
+    num_splits: int = 1
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+# The five workloads of the benchmark description, by what they are.
+WORKLOADS = {
+    "fwd_f32_single_head": Workload("fwd_f32_single_head", "fwd", 1, 1, 1, 256, 256, 64, "f32"),
+    "fwd_mha_n2048_d64": Workload("fwd_mha_n2048_d64", "fwd", 4, 16, 16, 2048, 2048, 64, "bf16"),
+    "fwd_causal_n8192_d128": Workload("fwd_causal_n8192_d128", "fwd", 2, 32, 32, 8192, 8192, 128,
+                                      "bf16", causal=True),
+    "bwd_causal_n4096_d128": Workload("bwd_causal_n4096_d128", "bwd", 2, 16, 16, 4096, 4096, 128,
+                                      "bf16", causal=True),
+    "decode_gqa_l4096": Workload("decode_gqa_l4096", "decode", 64, 32, 8, 1, 4096, 128, "bf16",
+                                 num_splits=16),
+}
+
+
+def make_inputs(w: Workload, *, Hkv: int | None = None, generator_seed: int | None = None):
+    """Seeded CPU tensors for workload ``w``.
+
+    fwd/bwd: q [B, Hq, Nq, d], k, v [B, Hkv, Nk, d] (+ do like q for bwd).
+    decode:  q [B, Hq, d], k, v [B, Hkv, L, d].
+    """
+    g = torch.Generator().manual_seed(w.seed if generator_seed is None else generator_seed)
+    hkv = w.Hkv if Hkv is None else Hkv
+    if w.kind == "decode":
+        q_shape = (w.B, w.Hq, w.d)
+    else:
+        q_shape = (w.B, w.Hq, w.Nq, w.d)
+    kv_shape = (w.B, hkv, w.Nk, w.d)
+    out = {
+        "q": torch.randn(q_shape, generator=g, dtype=torch.float32),
+        "k": torch.randn(kv_shape, generator=g, dtype=torch.float32),
+        "v": torch.randn(kv_shape, generator=g, dtype=torch.float32),
+    }
+    if w.kind == "bwd":
+        out["do"] = torch.randn(q_shape, generator=g, dtype=torch.float32)
+    return {k: t.to(w.torch_dtype) for k, t in out.items()}
+
+
+def random_like_shape(shape, dtype: torch.dtype, seed: int, scale: float = 1.0):
+    """N(0, scale²) draws of a given shape from a seeded CPU generator."""
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g, dtype=torch.float32) * scale).to(dtype)
+
+
+def to_f64(t: torch.Tensor):
+    """Exact upcast of a CPU or GPU tensor to a float64 NumPy array."""
+    return t.detach().to("cpu", torch.float64).numpy()
