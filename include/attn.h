@@ -1,0 +1,175 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) tiled exact-attention library.
+ *
+ * Every entry point computes exact softmax attention
+ *     O = softmax(scale · Q Kᵀ) V
+ * tile by tile with the online-softmax recurrence, as defined in the
+ * "Flash Attention 2" post (ahmadsaeedzaidi.github.io feed), sections
+ * "Standard Attention" (the definition) and "Flash Attention 2" (the inner
+ * loop: running row max m, running denominator l, accumulator rescaled by
+ * exp(m_old - m_new), one division by l at the end). The N×N score matrix
+ * never reaches device memory.
+ *
+ * Conventions shared by all calls
+ * -------------------------------
+ * Layout. Q, O, dO, dQ are [B, Hq, Nq, d]; K, V, dK, dV are [B, Hkv, Nk, d];
+ *   all contiguous, row-major, d innermost. LSE and the backward row term are
+ *   [B, Hq, Nq] float32. Decode uses q, o [B, Hq, d] and a KV cache
+ *   [B, Hkv, L, d] (the KVCache layout of the KV-compression post on
+ *   shreyansh26.github.io: batch, head, sequence, head_dim).
+ * GQA. Query head h reads KV head h / (Hq / Hkv) (contiguous groups, as the
+ *   KV-compression post's SnapKV code views heads); Hq % Hkv must be 0.
+ * LSE. Natural-log logsumexp of the scaled scores of each query row,
+ *   LSE = m + ln(l). A row with no visible key has O = 0 and LSE = -inf.
+ * Causal. Key j is visible to query i iff j <= i + (Nk - Nq) (bottom-right
+ *   alignment; at Nq == Nk this is the lower-triangular mask of the Flash
+ *   Attention 2 post, section "Causal masking"). Causal with Nq > Nk is
+ *   rejected.
+ * Pointers. All tensor pointers are DEVICE pointers owned by the caller.
+ *   The library allocates no memory and keeps no per-call state; scratch
+ *   space comes from the caller through the *_workspace_size() contract.
+ *   bf16 tensors must be 16-byte aligned; float32 tensors 16-byte aligned.
+ * Streams. `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream). All calls are asynchronous on that stream and return
+ *   after argument validation and launch. Arguments are validated before
+ *   anything is launched; on any error nothing is launched.
+ * Device-side waits. Every wait inside a kernel is bounded; a wait that runs
+ *   out sets a library error word and the kernel returns. attn_sync_status()
+ *   reports that as ATTN_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef ONLINE_SOFTMAX_TILED_GB300_ATTN_H
+#define ONLINE_SOFTMAX_TILED_GB300_ATTN_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1,     /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = -2,     /* valid but not implemented (head dim, dtype, ...)   */
+  ATTN_ERR_MISALIGNED = -3,      /* a tensor pointer is not 16-byte aligned             */
+  ATTN_ERR_WORKSPACE = -4,       /* workspace null or smaller than *_workspace_size()   */
+  ATTN_ERR_CUDA = -5,            /* a CUDA runtime call or kernel launch failed         */
+  ATTN_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait ran out                  */
+} attn_status;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * Forward pass with the row log-sum-exp.
+ *
+ * Flash Attention 2 post, section "Flash Attention 2", inner-loop steps 1-5
+ * and the final safe normalisation; the saved per-row statistic is the LSE
+ * (the attention-residuals kernel lab on manishklach.github.io saves the row
+ * max and denominator for the backward; LSE = max + ln(denominator) carries
+ * both). Scores are scaled by `scale` (1/sqrt(d) in the ML notes'
+ * attention Q&A on haolingpu.github.io).
+ *
+ * q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] in `dt`; o [B,Hq,Nq,d] written in `dt`;
+ * lse [B,Hq,Nq] float32 written (may be NULL to skip it).
+ * dt = ATTN_BF16: tcgen05 tensor-core path, d in {64, 128}; the probabilities
+ *   are rounded to bf16 for the P·V product, all softmax state is float32.
+ * dt = ATTN_F32:  float32 FFMA path (no TF32), d in {64, 128}.
+ * Returns ATTN_OK or an error listed above; nothing is launched on error.
+ */
+ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                     attn_dtype dt, void* stream);
+
+/*
+ * Bytes of device scratch attn_bwd needs: the row term D [B,Hq,Nq] float32
+ * and a float32 dQ accumulator [B,Hq,Nq,d], each 256-byte aligned.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+
+/*
+ * Backward pass by recomputation.
+ *
+ * Flash Attention 2 post, section "Flash Attention 2", "Recomputation in
+ * backward pass": S and P are rebuilt tile by tile from Q, K and the saved
+ * LSE, P = exp(scale·Q Kᵀ - LSE). The softmax step is the Jacobian-vector
+ * product of the softmax-backward note (shreyansh26.github.io), section
+ * "Backpropagating Through Softmax": dS = P ∘ (dP - D) with dP = dO Vᵀ and the
+ * row term D = rowsum(P ∘ dP), which equals rowsum(dO ∘ O) and is computed
+ * that way by a preprocess kernel. Then dV = Pᵀ dO, dK = scale·dSᵀ Q and
+ * dQ = scale·dS K; dQ is accumulated in float32 (the attention-residuals lab
+ * reduces multi-writer gradients through float32 atomics) and converted at
+ * the end. With GQA, dK and dV of a KV head sum over its query heads.
+ *
+ * Inputs: q, k, v, o (forward output), dO, lse (forward LSE), all in `dt`
+ * except lse (float32). Outputs dq, dk, dv in `dt`, overwritten.
+ * workspace: device scratch of at least attn_bwd_workspace_size() bytes,
+ * 256-byte aligned; its contents on entry do not matter.
+ * dt = ATTN_BF16 with d in {64, 128}; ATTN_F32 with d in {64, 128}.
+ */
+ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                     attn_dtype dt, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Bytes of device scratch attn_decode_splitkv needs: per (b, query head,
+ * split) the partial triple (o [d], m, l) in float32, 256-byte aligned.
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * Split-KV decode (query length 1) with an exact merge.
+ *
+ * ML notes (haolingpu.github.io), split-K kernel notes: the KV axis of each
+ * request is cut into `num_splits` chunks processed by independent blocks;
+ * each chunk leaves its maximum score m_s, un-normalised denominator
+ * l_s = Σ exp(s - m_s) and un-normalised output o_s = Σ exp(s - m_s) v in the
+ * workspace; a second kernel rescales every chunk onto the common maximum and
+ * merges them exactly, in any order. Chunk s covers keys
+ * [s*c, min((s+1)*c, L)), c = ceil(L / num_splits); an empty chunk carries
+ * zero mass (attention-residuals lab, "Phase 2").
+ *
+ * q [B,Hq,d] bf16, k_cache/v_cache [B,Hkv,L,d] bf16; o [B,Hq,d] bf16 written;
+ * lse [B,Hq] float32 written (may be NULL). d must be 128 or 64; Hq/Hkv <= 8.
+ * workspace: at least attn_decode_workspace_size() bytes, 256-byte aligned.
+ */
+ATTN_API attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                                void* o, float* lse, int B, int Hq, int Hkv, int L, int d,
+                                float scale, int num_splits, void* workspace, size_t ws_bytes,
+                                void* stream);
+
+/*
+ * The exact (o, m, l) merge on its own (ML notes, split-K notes; the
+ * attention-residuals lab, "Phase 2: merge the live partial exactly").
+ *
+ * o_part [rows, num_splits, d], m_part and l_part [rows, num_splits], all
+ * float32, with o un-normalised (o_s = Σ exp(s - m_s) v). Writes
+ * o [rows, d] in `out_dt` = Σ_s e^(m_s - m) o_s / Σ_s e^(m_s - m) l_s with
+ * m = max_s m_s, and lse [rows] = m + ln(l) (lse may be NULL). A split with
+ * m_s = -inf contributes nothing; a row with no mass gets O = 0, LSE = -inf.
+ * d must be a multiple of 4 and at most 256.
+ */
+ATTN_API attn_status attn_merge_partials(const float* o_part, const float* m_part, const float* l_part,
+                                void* o, float* lse, int rows, int num_splits, int d,
+                                attn_dtype out_dt, void* stream);
+
+/* Static, human-readable name of a status code. */
+ATTN_API const char* attn_status_string(attn_status s);
+
+/*
+ * Synchronise `stream`, then report (and clear) the library's device error
+ * word: ATTN_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the
+ * last check, ATTN_ERR_CUDA if the stream reports a CUDA error, else ATTN_OK.
+ */
+ATTN_API attn_status attn_sync_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ONLINE_SOFTMAX_TILED_GB300_ATTN_H */

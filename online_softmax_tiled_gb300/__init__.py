@@ -1,0 +1,27 @@
+"""GB300 (sm_103a) tiled exact softmax attention with the online-softmax
+recurrence: forward with LSE, recomputing backward, split-KV decode and the
+exact (o, m, l) merge, behind the C ABI of ``include/attn.h``.
+
+The Python layer only marshals torch tensors into that ABI; the computation
+runs in the library's CUDA kernels.
+"""
+
+from ._binding import (  # noqa: F401
+    ATTN_BF16,
+    ATTN_F32,
+    ATTN_OK,
+    AttnError,
+    attn_bwd,
+    attn_bwd_workspace_size,
+    attn_decode_splitkv,
+    attn_decode_workspace_size,
+    attn_fwd,
+    attn_merge_partials,
+    attn_status_string,
+    attn_sync_status,
+    backward,
+    decode,
+    forward,
+    lib,
+)
+from ._build import LIB_PATH, build  # noqa: F401

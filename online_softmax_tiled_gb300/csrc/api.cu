@@ -1,0 +1,178 @@
+// C ABI entry points: argument validation, workspace carving and dispatch to
+// the kernel launchers. Declarations and their documentation: include/attn.h.
+
+#include <stdint.h>
+
+#include "common.cuh"
+#include "launchers.h"
+
+using namespace attn;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+attn_status check_attention_shapes(int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal,
+                                   attn_dtype dt) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return ATTN_ERR_INVALID_ARG;
+  if (dt != ATTN_F32 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  // index arithmetic inside the kernels uses 32-bit row counts per head
+  if ((long long)B * Hq * Nq > (1LL << 31) || (long long)B * Hkv * Nk > (1LL << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+struct BwdLayout {
+  size_t row_term, dq_acc, total;
+};
+
+BwdLayout bwd_layout(int B, int Hq, int Nq, int d) {
+  BwdLayout l;
+  const size_t rows = size_t(B) * Hq * Nq;
+  l.row_term = 0;
+  l.dq_acc = align256(rows * sizeof(float));
+  l.total = l.dq_acc + align256(rows * d * sizeof(float));
+  return l;
+}
+
+struct DecodeLayout {
+  size_t o_part, m_part, l_part, total;
+};
+
+DecodeLayout decode_layout(int B, int Hq, int d, int S) {
+  DecodeLayout l;
+  const size_t n = size_t(B) * Hq * S;
+  l.o_part = 0;
+  l.m_part = align256(n * d * sizeof(float));
+  l.l_part = l.m_part + align256(n * sizeof(float));
+  l.total = l.l_part + align256(n * sizeof(float));
+  return l;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer (16-byte alignment required)";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                     attn_dtype dt, void* stream) {
+  attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, causal, dt);
+  if (st != ATTN_OK) return st;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;  // NaN scale
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && !aligned16(lse)))
+    return ATTN_ERR_MISALIGNED;
+  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, dt,
+            static_cast<cudaStream_t>(stream)};
+  if (dt == ATTN_BF16) return from_cuda(launch_fwd_tc(a));
+  return from_cuda(launch_fwd_simt(a));
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
+  (void)Hkv;
+  (void)Nk;
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || d <= 0) return 0;
+  return bwd_layout(B, Hq, Nq, d).total;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, attn_dtype dt,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, causal, dt);
+  if (st != ATTN_OK) return st;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return ATTN_ERR_MISALIGNED;
+  const BwdLayout lay = bwd_layout(B, Hq, Nq, d);
+  if (!workspace || ws_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  char* ws = static_cast<char*>(workspace);
+  BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, dt,
+            reinterpret_cast<float*>(ws + lay.row_term), reinterpret_cast<float*>(ws + lay.dq_acc),
+            static_cast<cudaStream_t>(stream)};
+  cudaError_t e = launch_bwd_preprocess(a);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = (dt == ATTN_BF16) ? launch_bwd_tc(a) : launch_bwd_simt(a);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return from_cuda(launch_bwd_convert(a));
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
+  if (B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
+  return decode_layout(B, Hq, d, num_splits).total;
+}
+
+attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, void* o,
+                                float* lse, int B, int Hq, int Hkv, int L, int d, float scale,
+                                int num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || d <= 0 || num_splits <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !o) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
+  if (num_splits > 65535 || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (lse && !aligned16(lse)))
+    return ATTN_ERR_MISALIGNED;
+  const DecodeLayout lay = decode_layout(B, Hq, d, num_splits);
+  if (!workspace || ws_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  char* ws = static_cast<char*>(workspace);
+  DecodeArgs a{q, k_cache, v_cache, o, lse, B, Hq, Hkv, L, d, scale, num_splits,
+               reinterpret_cast<float*>(ws + lay.o_part), reinterpret_cast<float*>(ws + lay.m_part),
+               reinterpret_cast<float*>(ws + lay.l_part), static_cast<cudaStream_t>(stream)};
+  cudaError_t e = launch_decode_split(a);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  MergeArgs m{a.o_part, a.m_part, a.l_part, o, lse, B * Hq, num_splits, d, ATTN_BF16, a.stream};
+  return from_cuda(launch_merge(m));
+}
+
+attn_status attn_merge_partials(const float* o_part, const float* m_part, const float* l_part,
+                                void* o, float* lse, int rows, int num_splits, int d,
+                                attn_dtype out_dt, void* stream) {
+  if (rows <= 0 || num_splits <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!o_part || !m_part || !l_part || !o) return ATTN_ERR_INVALID_ARG;
+  if (out_dt != ATTN_F32 && out_dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d % 4 != 0 || d > 256) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o_part) || !aligned16(o)) return ATTN_ERR_MISALIGNED;
+  MergeArgs m{o_part, m_part, l_part, o, lse, rows, num_splits, d, out_dt,
+              static_cast<cudaStream_t>(stream)};
+  return from_cuda(launch_merge(m));
+}
+
+attn_status attn_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  const uint32_t w = take_error_fwd_tc() | take_error_bwd_tc() | take_error_decode();
+  if (w == 0xffffffffu) return ATTN_ERR_CUDA;
+  if (w & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+  return ATTN_OK;
+}
+
+}  // extern "C"

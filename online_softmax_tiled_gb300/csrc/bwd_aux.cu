@@ -1,0 +1,88 @@
+// Backward helpers: the row-term preprocess and the dQ conversion.
+//
+// Row term. The softmax-backward note (shreyansh26.github.io feed), section
+// "Backpropagating Through Softmax", writes the softmax Jacobian-vector
+// product as P ∘ (dP - rowsum(P ∘ dP)). With O = P V and dP = dO Vᵀ,
+// rowsum(P ∘ dP) = Σ_j P_ij Σ_c dO_ic V_jc = Σ_c dO_ic O_ic, so the row term
+// D_i = rowsum(dO ∘ O) is computed here from O and dO in one streaming pass,
+// before the main backward kernel runs. The same pass zeroes the float32 dQ
+// accumulator that the main kernel adds into.
+//
+// dQ conversion. After the main kernel, dQ = dtype(dQ_acc) (round to nearest
+// even for bf16).
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace attn {
+namespace {
+
+// One warp per query row; lane l handles columns l, l+32, ... (coalesced).
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO,
+                      float* __restrict__ row_term, float* __restrict__ dq_acc, long rows) {
+  const long row = long(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const T* orow = o + row * D;
+  const T* grow = dO + row * D;
+  float acc = 0.f;
+#pragma unroll
+  for (int c = lane; c < D; c += 32) acc = fmaf(to_f32(orow[c]), to_f32(grow[c]), acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) row_term[row] = acc;
+  float* qrow = dq_acc + row * D;
+#pragma unroll
+  for (int c = lane; c < D; c += 32) qrow[c] = 0.f;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+bwd_convert_kernel(const float4* __restrict__ src, T* __restrict__ dst, long n4) {
+  for (long i = long(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += long(gridDim.x) * blockDim.x) {
+    const float4 x = src[i];
+    T* d = dst + 4 * i;
+    d[0] = from_f32<T>(x.x);
+    d[1] = from_f32<T>(x.y);
+    d[2] = from_f32<T>(x.z);
+    d[3] = from_f32<T>(x.w);
+  }
+}
+
+template <typename T>
+cudaError_t launch_pre_t(const BwdArgs& a) {
+  const long rows = long(a.B) * a.Hq * a.Nq;
+  const unsigned blocks = unsigned((rows + 7) / 8);
+  if (a.d == 64)
+    bwd_preprocess_kernel<T, 64><<<blocks, 256, 0, a.stream>>>(
+        static_cast<const T*>(a.o), static_cast<const T*>(a.dO), a.row_term, a.dq_acc, rows);
+  else
+    bwd_preprocess_kernel<T, 128><<<blocks, 256, 0, a.stream>>>(
+        static_cast<const T*>(a.o), static_cast<const T*>(a.dO), a.row_term, a.dq_acc, rows);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_convert_t(const BwdArgs& a) {
+  const long n4 = long(a.B) * a.Hq * a.Nq * a.d / 4;
+  long blocks = (n4 + 255) / 256;
+  if (blocks > 152L * 16) blocks = 152L * 16;
+  bwd_convert_kernel<T><<<unsigned(blocks), 256, 0, a.stream>>>(
+      reinterpret_cast<const float4*>(a.dq_acc), static_cast<T*>(a.dq), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const BwdArgs& a) {
+  return a.dt == ATTN_F32 ? launch_pre_t<float>(a) : launch_pre_t<__nv_bfloat16>(a);
+}
+
+cudaError_t launch_bwd_convert(const BwdArgs& a) {
+  return a.dt == ATTN_F32 ? launch_convert_t<float>(a) : launch_convert_t<__nv_bfloat16>(a);
+}
+
+}  // namespace attn

@@ -1,0 +1,140 @@
+// Shared device/host helpers for the sm_103a attention kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+#define ATTN_DEVINL __device__ __forceinline__
+
+namespace attn {
+
+// ----------------------------------------------------------------------------
+// Error word. Each translation unit owns one (kernels in different units are
+// compiled without relocatable device code, so a single shared __device__
+// variable is not possible); the host polls all of them in attn_sync_status.
+// Bits: 1 = a bounded wait ran out.
+// ----------------------------------------------------------------------------
+enum : uint32_t { kErrTimeout = 1u };
+
+#define ATTN_DEFINE_ERROR_WORD(fn_name)                                          \
+  static __device__ uint32_t g_attn_err_word;                                  \
+  ATTN_DEVINL void attn_flag_error(uint32_t bits) {                            \
+    atomicOr(&g_attn_err_word, bits);                                          \
+  }                                                                            \
+  uint32_t fn_name() {                                                         \
+    uint32_t v = 0, zero = 0;                                                  \
+    if (cudaMemcpyFromSymbol(&v, g_attn_err_word, sizeof(v)) != cudaSuccess)   \
+      return 0xffffffffu;                                                      \
+    if (v) cudaMemcpyToSymbol(g_attn_err_word, &zero, sizeof(zero));           \
+    return v;                                                                  \
+  }
+
+// ----------------------------------------------------------------------------
+// Small numeric helpers
+// ----------------------------------------------------------------------------
+ATTN_DEVINL float to_f32(float x) { return x; }
+ATTN_DEVINL float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> ATTN_DEVINL T from_f32(float x);
+template <> ATTN_DEVINL float from_f32<float>(float x) { return x; }
+template <> ATTN_DEVINL __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// 2^x on the special-function unit (ex2.approx, relative error ~2^-22).
+ATTN_DEVINL float fast_exp2(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Pack two floats into a bf16x2 word, round-to-nearest-even; `lo` goes to the
+// low half (the lower-addressed element).
+ATTN_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+ATTN_DEVINL float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+ATTN_DEVINL float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+ATTN_DEVINL uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Upper bound on any single device-side wait. Legitimate waits in these
+// kernels last microseconds; anything near this limit is a bug or a hang.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ----------------------------------------------------------------------------
+// mbarrier helpers (shared::cta addresses as 32-bit)
+// ----------------------------------------------------------------------------
+ATTN_DEVINL uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+ATTN_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+ATTN_DEVINL void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+ATTN_DEVINL void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+ATTN_DEVINL void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+
+ATTN_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+      ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+ATTN_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`. Returns false if it ran out (or if
+// `*abort` was raised by another thread of the CTA while waiting).
+ATTN_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.
+// Both addresses 16-byte aligned, size a multiple of 16.
+// ----------------------------------------------------------------------------
+ATTN_DEVINL void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace attn

@@ -1,0 +1,344 @@
+// Split-KV decode and the exact (o, m, l) merge.
+//
+// ML notes (haolingpu.github.io), split-K kernel notes: the KV axis of one
+// request is cut into S chunks so that more blocks run at once; each chunk
+// leaves its maximum score m_s, un-normalised denominator
+// l_s = Σ exp(s - m_s) and un-normalised output o_s = Σ exp(s - m_s) v in
+// global scratch, and a second kernel rescales every chunk by exp(m_s - m)
+// onto the common maximum m and merges them exactly, in any order. An empty
+// chunk has m_s = -inf and carries zero mass (attention-residuals kernel
+// lab, manishklach.github.io, "Phase 2").
+//
+// Split kernel. Decode is bound by reading the KV cache once (about 4 flops
+// per byte), so it runs on the FMA pipes, not the tensor cores. One CTA owns
+// (request b, KV head g, chunk s) and all G = Hq/Hkv query heads that share
+// that KV head, so every K/V byte is read from HBM exactly once. K and V
+// rows of the chunk stream through a 4-stage shared-memory ring filled by
+// bulk asynchronous copies (each stage is a contiguous run of rows, so one
+// copy per tensor per stage). Eight consecutive lanes own one key: lane
+// `sub` holds dims {64v + 8sub .. 64v + 8sub + 7}, so a warp's 16-byte
+// shared loads cover whole 128-byte rows without bank conflicts. Each 8-lane
+// group runs its own online softmax over its keys; the 16 groups of the CTA
+// are merged with the same exact rule at the end.
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace attn {
+
+ATTN_DEFINE_ERROR_WORD(take_error_decode)
+
+namespace {
+
+constexpr int kThreads = 128;     // 4 warps, 16 key groups of 8 lanes
+constexpr int kStageKeys = 32;    // keys per pipeline stage
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int G>
+constexpr size_t decode_smem_bytes() {
+  // K and V ring; the final cross-group merge (16 groups × G heads of
+  // (m, l, o[D]) in float32) reuses it.
+  constexpr size_t ring = size_t(2) * kStages * kStageKeys * D * 2;
+  constexpr size_t merge = size_t(16) * G * (D + 2) * 4;
+  return ring > merge ? ring : merge;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads)
+decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                    const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
+                    float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
+                    int L, int S, float scale) {
+  constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
+  constexpr int kRowBytes = D * 2;
+  constexpr int kStageBytes = kStageKeys * kRowBytes;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + kStages * kStageBytes;
+  __shared__ uint64_t full_bar[kStages];
+  __shared__ int abort_flag;
+
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = lane >> 3, sub = lane & 7;
+  const int chunk = (L + S - 1) / S;
+  const int key_begin = min(L, s * chunk);
+  const int key_end = min(L, key_begin + chunk);
+  const int nkeys = key_end - key_begin;
+  const int nstages = (nkeys + kStageKeys - 1) / kStageKeys;
+
+  const size_t kv_off = (size_t(b) * Hkv + g) * size_t(L) * D;
+  const uint8_t* kg = reinterpret_cast<const uint8_t*>(k + kv_off) + size_t(key_begin) * kRowBytes;
+  const uint8_t* vg = reinterpret_cast<const uint8_t*>(v + kv_off) + size_t(key_begin) * kRowBytes;
+
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int st) {
+    const int buf = st % kStages;
+    const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+    const uint32_t bytes = uint32_t(rows) * kRowBytes;
+    mbar_arrive_expect_tx(&full_bar[buf], 2 * bytes);
+    bulk_g2s(sK + buf * kStageBytes, kg + size_t(st) * kStageBytes, bytes, &full_bar[buf]);
+    bulk_g2s(sV + buf * kStageBytes, vg + size_t(st) * kStageBytes, bytes, &full_bar[buf]);
+  };
+  int issued = 0;  // meaningful in thread 0 only
+  if (tid == 0)
+    for (; issued < min(kStages, nstages); ++issued) issue(issued);
+
+  // Query slice of this lane for all G heads, pre-scaled into log2 units.
+  float qf[G][NV * 8];
+  const float qs = scale * kLog2e;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const __nv_bfloat16* qh = q + (size_t(b) * Hq + g * G + h) * D;
+#pragma unroll
+    for (int vv = 0; vv < NV; ++vv) {
+      const uint4 w = *reinterpret_cast<const uint4*>(qh + 64 * vv + 8 * sub);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        qf[h][vv * 8 + 2 * e] = bf16lo(ws[e]) * qs;
+        qf[h][vv * 8 + 2 * e + 1] = bf16hi(ws[e]) * qs;
+      }
+    }
+  }
+
+  float acc[G][NV * 8];
+  float m_run[G], l_run[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < NV * 8; ++e) acc[h][e] = 0.f;
+  }
+
+  bool ok = true;
+  for (int st = 0; st < nstages; ++st) {
+    const int buf = st % kStages;
+    const bool fail = !mbar_wait_bounded(&full_bar[buf], (st / kStages) & 1, &abort_flag);
+    if (fail) abort_flag = 1;
+    // One barrier per stage: all threads agree on failure, and the buffer of
+    // stage st-1 is free once every thread has arrived here.
+    if (__syncthreads_or(fail)) {
+      if (tid == 0) {
+        attn_flag_error(kErrTimeout);
+        // Let copies already issued land before shared memory goes away.
+        for (int t = st; t < issued; ++t)
+          mbar_wait_bounded(&full_bar[t % kStages], (t / kStages) & 1, nullptr);
+      }
+      ok = false;
+      break;
+    }
+    if (tid == 0 && issued < nstages && st >= 1) issue(issued++);
+    const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+    const uint8_t* kb = sK + buf * kStageBytes;
+    const uint8_t* vb = sV + buf * kStageBytes;
+
+    // This group's two keys of the stage: warp*8 + grp and warp*8 + grp + 4.
+    float sc[2][G];
+    uint4 vrow[2][NV];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int kk = warp * 8 + grp + 4 * r;
+      const bool valid = kk < rows;
+      const int kr = valid ? kk : 0;
+      float part[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) part[h] = 0.f;
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv) {
+        const uint4 w = *reinterpret_cast<const uint4*>(kb + kr * kRowBytes + (64 * vv + 8 * sub) * 2);
+        vrow[r][vv] = *reinterpret_cast<const uint4*>(vb + kr * kRowBytes + (64 * vv + 8 * sub) * 2);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float k0 = bf16lo(ws[e]), k1 = bf16hi(ws[e]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            part[h] = fmaf(qf[h][vv * 8 + 2 * e], k0, part[h]);
+            part[h] = fmaf(qf[h][vv * 8 + 2 * e + 1], k1, part[h]);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float x = part[h];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        sc[r][h] = valid ? x : -INFINITY;
+      }
+    }
+
+    // Online update of (m, l, o) for this group's two keys.
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float m_new = fmaxf(m_run[h], fmaxf(sc[0][h], sc[1][h]));
+      if (m_new == -INFINITY) continue;  // nothing visible yet in this group
+      const float alpha = fast_exp2(m_run[h] - m_new);   // 0 when m_run = -inf
+      const float p0 = fast_exp2(sc[0][h] - m_new);
+      const float p1 = fast_exp2(sc[1][h] - m_new);
+      l_run[h] = fmaf(alpha, l_run[h], p0 + p1);
+      m_run[h] = m_new;
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv) {
+        const uint32_t w0[4] = {vrow[0][vv].x, vrow[0][vv].y, vrow[0][vv].z, vrow[0][vv].w};
+        const uint32_t w1[4] = {vrow[1][vv].x, vrow[1][vv].y, vrow[1][vv].z, vrow[1][vv].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float& a0 = acc[h][vv * 8 + 2 * e];
+          float& a1 = acc[h][vv * 8 + 2 * e + 1];
+          a0 = fmaf(p1, bf16lo(w1[e]), fmaf(p0, bf16lo(w0[e]), a0 * alpha));
+          a1 = fmaf(p1, bf16hi(w1[e]), fmaf(p0, bf16hi(w0[e]), a1 * alpha));
+        }
+      }
+    }
+
+  }
+  if (!ok) return;
+
+  // Cross-group merge: 16 groups × G heads, exact rescale onto the common max.
+  __syncthreads();
+  float* sm_m = reinterpret_cast<float*>(smem);                 // [16][G]
+  float* sm_l = sm_m + 16 * G;                                  // [16][G]
+  float* sm_o = sm_l + 16 * G;                                  // [16][G][D]
+  const int gid = warp * 4 + grp;
+  if (sub == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      sm_m[gid * G + h] = m_run[h];
+      sm_l[gid * G + h] = l_run[h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int vv = 0; vv < NV; ++vv)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm_o[(gid * G + h) * D + 64 * vv + 8 * sub + e] = acc[h][vv * 8 + e];
+  __syncthreads();
+
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int h = idx / D, c = idx % D;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) mx = fmaxf(mx, sm_m[t * G + h]);
+    float o = 0.f, l = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float mt = sm_m[t * G + h];
+        const float w = (mt == -INFINITY) ? 0.f : fast_exp2(mt - mx);
+        o = fmaf(w, sm_o[(t * G + h) * D + c], o);
+        l = fmaf(w, sm_l[t * G + h], l);
+      }
+    }
+    const size_t row = size_t(b) * Hq + g * G + h;
+    o_part[(row * S + s) * D + c] = o;
+    if (c == 0) {
+      m_part[row * S + s] = (mx == -INFINITY) ? -INFINITY : mx * kLn2;  // back to natural units
+      l_part[row * S + s] = l;
+    }
+  }
+}
+
+// One warp per output row; lane owns float4 column groups lane, lane+32, ...
+template <typename TOut>
+__global__ void __launch_bounds__(256)
+merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
+             const float* __restrict__ l_part, TOut* __restrict__ o, float* __restrict__ lse,
+             int rows, int S, int d) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float* mr = m_part + size_t(row) * S;
+  const float* lr = l_part + size_t(row) * S;
+  float mx = -INFINITY;
+  for (int t = lane; t < S; t += 32) mx = fmaxf(mx, mr[t]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float l = 0.f;
+  if (mx != -INFINITY)
+    for (int t = lane; t < S; t += 32) {
+      const float mt = mr[t];
+      if (mt != -INFINITY) l = fmaf(expf(mt - mx), lr[t], l);
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  const bool empty = !(l > 0.f);
+  const float inv = empty ? 0.f : 1.f / l;
+  for (int c4 = lane; c4 < d / 4; c4 += 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!empty)
+      for (int t = 0; t < S; ++t) {
+        const float mt = mr[t];
+        if (mt == -INFINITY) continue;
+        const float w = expf(mt - mx);
+        const float4 x = reinterpret_cast<const float4*>(o_part + (size_t(row) * S + t) * d)[c4];
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+    TOut* orow = o + size_t(row) * d + 4 * c4;
+    orow[0] = from_f32<TOut>(acc.x * inv);
+    orow[1] = from_f32<TOut>(acc.y * inv);
+    orow[2] = from_f32<TOut>(acc.z * inv);
+    orow[3] = from_f32<TOut>(acc.w * inv);
+  }
+  if (lse != nullptr && lane == 0) lse[row] = empty ? -INFINITY : mx + logf(l);
+}
+
+template <int D, int G>
+cudaError_t launch_split_t(const DecodeArgs& a) {
+  const size_t smem = decode_smem_bytes<D, G>();
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_splits, a.Hkv, a.B);
+  decode_split_kernel<D, G><<<grid, kThreads, smem, a.stream>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+      static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part, a.Hq, a.Hkv, a.L,
+      a.num_splits, a.scale);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_split_d(const DecodeArgs& a) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_split_t<D, 1>(a);
+    case 2: return launch_split_t<D, 2>(a);
+    case 4: return launch_split_t<D, 4>(a);
+    case 8: return launch_split_t<D, 8>(a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_split(const DecodeArgs& a) {
+  return a.d == 64 ? launch_split_d<64>(a) : launch_split_d<128>(a);
+}
+
+cudaError_t launch_merge(const MergeArgs& a) {
+  const unsigned blocks = unsigned((a.rows + 7) / 8);
+  if (a.out_dt == ATTN_F32)
+    merge_kernel<float><<<blocks, 256, 0, a.stream>>>(a.o_part, a.m_part, a.l_part,
+                                                      static_cast<float*>(a.o), a.lse, a.rows,
+                                                      a.num_splits, a.d);
+  else
+    merge_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(
+        a.o_part, a.m_part, a.l_part, static_cast<__nv_bfloat16*>(a.o), a.lse, a.rows,
+        a.num_splits, a.d);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

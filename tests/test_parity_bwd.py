@@ -1,0 +1,74 @@
+"""GPU backward vs the float64 oracle (JVP route), element by element.
+
+Tolerance (from the benchmark description, written here): per gradient
+tensor, max|err| <= 5e-2 * max|ref| for bf16 inputs with float32
+accumulation; 1e-4 * max|ref| for float32 inputs. The GPU takes O and LSE
+from its own forward, as a training step would.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, Workload, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _grads(ost, w, scale=None):
+    x = {k: t.to(DEV) for k, t in make_inputs(w).items()}
+    scale = w.scale if scale is None else scale
+    o, lse = ost.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=scale)
+    dq, dk, dv = ost.backward(x["q"], x["k"], x["v"], o, x["do"], lse, causal=w.causal,
+                              scale=scale)
+    torch.cuda.synchronize()
+    return x, (dq, dk, dv), scale
+
+
+def _rel_tol(dtype):
+    return 5e-2 if dtype == "bf16" else 1e-4
+
+
+SMALL = [
+    (1, 2, 2, 200, 200, 64, "bf16", True),
+    (1, 2, 2, 300, 300, 128, "bf16", False),
+    (1, 4, 2, 257, 257, 128, "bf16", True),      # GQA: dK, dV sum over the group
+    (1, 2, 2, 130, 390, 64, "bf16", True),       # Nq < Nk
+    (2, 2, 2, 64, 64, 128, "bf16", True),
+    (1, 1, 1, 1, 77, 64, "bf16", False),
+    (1, 2, 2, 100, 100, 64, "f32", True),
+    (1, 4, 1, 90, 150, 128, "f32", False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dtype,causal", SMALL)
+def test_small_shapes(ost, B, Hq, Hkv, Nq, Nk, d, dtype, causal):
+    w = Workload("small", "bwd", B, Hq, Hkv, Nq, Nk, d, dtype, causal, seed=Nq * 7 + Nk)
+    x, got, scale = _grads(ost, w)
+    ref = oracle.attention_bwd(*(to_f64(x[n]) for n in ("q", "k", "v", "do")), scale, causal)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        err = np.max(np.abs(to_f64(g) - r))
+        assert err <= _rel_tol(dtype) * np.max(np.abs(r)), (name, err, np.max(np.abs(r)))
+
+
+def test_peaked_rows(ost):
+    w = Workload("peaked", "bwd", 1, 2, 2, 256, 256, 128, "bf16", True, seed=21)
+    x, got, scale = _grads(ost, w, scale=8.0 / np.sqrt(128))
+    ref = oracle.attention_bwd(*(to_f64(x[n]) for n in ("q", "k", "v", "do")), scale, True)
+    for g, r in zip(got, ref):
+        assert np.max(np.abs(to_f64(g) - r)) <= 5e-2 * np.max(np.abs(r))
+
+
+def test_causal_backward_workload_sampled_heads(ost):
+    """B=2, H=16, N=4096, d=128 causal bf16 at full size; the oracle computes
+    whole heads (dK, dV of a head need every query row of it)."""
+    w = WORKLOADS["bwd_causal_n4096_d128"]
+    x, got, scale = _grads(ost, w)
+    for b, h in [(0, 0), (1, 15)]:
+        sl = lambda t: to_f64(t[b:b + 1, h:h + 1])
+        ref = oracle.attention_bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), scale, True)
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            err = np.max(np.abs(sl(g) - r))
+            assert err <= 5e-2 * np.max(np.abs(r)), (name, b, h, err)

@@ -1,0 +1,81 @@
+"""GPU split-KV decode and merge vs the float64 oracle.
+
+Tolerance: bf16 O max|err| <= 2e-2, LSE <= 1e-3 (benchmark description);
+the merge kernel on float32 partials: 1e-5 relative to max|O|.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, Workload, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _check(ost, w, scale=None):
+    x = {k: t.to(DEV) for k, t in make_inputs(w).items()}
+    scale = w.scale if scale is None else scale
+    o, lse = ost.decode(x["q"], x["k"], x["v"], w.num_splits, scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_splitkv(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), scale,
+                                           w.num_splits)
+    err_o = np.max(np.abs(to_f64(o) - o_ref))
+    assert err_o <= 2e-2, err_o
+    assert np.max(np.abs(to_f64(lse) - lse_ref)) <= 1e-3
+    return err_o, np.max(np.abs(o_ref))
+
+
+def test_gqa_decode_workload_full(ost):
+    """B=64, Hq=32, Hkv=8, d=128, L=4096, 16 splits: every output row."""
+    _check(ost, WORKLOADS["decode_gqa_l4096"])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,L,d,S", [
+    (2, 8, 2, 300, 128, 7),
+    (1, 4, 4, 50, 64, 16),
+    (3, 16, 2, 1000, 128, 3),     # group of 8
+    (2, 4, 2, 5, 128, 16),        # splits 5..15 are empty
+    (1, 2, 1, 1, 64, 1),
+    (1, 8, 8, 4096, 128, 1),      # one split covers everything
+    (4, 32, 8, 777, 64, 5),
+])
+def test_small_shapes(ost, B, Hq, Hkv, L, d, S):
+    _check(ost, Workload("small", "decode", B, Hq, Hkv, 1, L, d, "bf16", num_splits=S, seed=L + S))
+
+
+def test_peaked_scores(ost):
+    w = Workload("peaked", "decode", 4, 8, 2, 1, 1024, 128, "bf16", num_splits=8, seed=9)
+    err, ref_max = _check(ost, w, scale=8.0 / np.sqrt(128))
+    assert err <= 1e-2 * ref_max
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_merge_kernel_permuted_and_empty_splits(ost, out_dtype):
+    w = Workload("merge", "decode", 3, 4, 2, 1, 200, 64, "bf16", num_splits=6, seed=17)
+    x = make_inputs(w)
+    o_p, m_p, l_p = oracle.decode_split_partials(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]),
+                                                  w.scale, w.num_splits)
+    rows = w.B * w.Hq
+    o_p, m_p, l_p = o_p.reshape(rows, 6, 64), m_p.reshape(rows, 6), l_p.reshape(rows, 6)
+    perm = np.random.default_rng(1).permutation(6)
+    o_p, m_p, l_p = o_p[:, perm], m_p[:, perm], l_p[:, perm]
+    # two empty splits per row and one row with no mass at all
+    o_p = np.concatenate([o_p, np.zeros((rows, 2, 64))], axis=1)
+    m_p = np.concatenate([m_p, np.full((rows, 2), -np.inf)], axis=1)
+    l_p = np.concatenate([l_p, np.zeros((rows, 2))], axis=1)
+    o_p[5], m_p[5], l_p[5] = 0.0, -np.inf, 0.0
+    o_ref, lse_ref = oracle.merge_partials(o_p, m_p, l_p)
+    t = lambda a: torch.tensor(a, dtype=torch.float32, device=DEV).contiguous()
+    o = torch.empty((rows, 64), dtype=out_dtype, device=DEV)
+    lse = torch.empty(rows, dtype=torch.float32, device=DEV)
+    ost.attn_merge_partials(t(o_p), t(m_p), t(l_p), o, lse)
+    torch.cuda.synchronize()
+    tol = 1e-5 * np.max(np.abs(o_ref)) if out_dtype == torch.float32 else 1e-2
+    assert np.max(np.abs(to_f64(o) - o_ref)) <= tol
+    got_lse = to_f64(lse)
+    assert np.isneginf(got_lse[5]) and np.all(to_f64(o)[5] == 0)
+    fin = np.isfinite(lse_ref)
+    assert np.max(np.abs(got_lse[fin] - lse_ref[fin])) <= 1e-5

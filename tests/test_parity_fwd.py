@@ -1,0 +1,108 @@
+"""GPU forward vs the float64 oracle, element by element.
+
+Tolerances (from the benchmark description, written here): float32 inputs
+max|err| <= 1e-5 on O and LSE; bf16 inputs max|err| <= 2e-2 on O and
+<= 1e-3 on LSE. Because N(0,1) inputs with scale 1/sqrt(d) give nearly
+uniform rows (|O| of a few hundredths), the bf16 cases also run with peaked
+rows (scale x8) and the error is reported relative to max|O|.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, Workload, make_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _tol(dtype):
+    return (1e-5, 1e-5) if dtype == "f32" else (2e-2, 1e-3)
+
+
+def _run(ost, w, scale=None, with_lse=True):
+    x = {k: t.to(DEV) for k, t in make_inputs(w).items()}
+    scale = w.scale if scale is None else scale
+    o, lse = ost.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=scale, with_lse=with_lse)
+    torch.cuda.synchronize()
+    return x, o, lse, scale
+
+
+def _check_full(ost, w, scale=None):
+    x, o, lse, scale = _run(ost, w, scale)
+    o_ref, lse_ref = oracle.attention_fwd(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), scale,
+                                          w.causal)
+    tol_o, tol_l = _tol(w.dtype)
+    err_o = np.max(np.abs(to_f64(o) - o_ref))
+    err_l = np.max(np.abs(to_f64(lse) - lse_ref))
+    assert err_o <= tol_o, (err_o, np.max(np.abs(o_ref)))
+    assert err_l <= tol_l, err_l
+    return err_o, err_l
+
+
+def test_f32_single_head_workload(ost):
+    _check_full(ost, WORKLOADS["fwd_f32_single_head"])
+
+
+SMALL = [
+    # B, Hq, Hkv, Nq, Nk, d, dtype, causal
+    (1, 2, 2, 300, 300, 64, "bf16", False),
+    (1, 2, 2, 300, 300, 128, "bf16", True),
+    (2, 4, 1, 257, 513, 128, "bf16", True),     # GQA 4:1, Nq < Nk, ragged tails
+    (1, 3, 3, 129, 129, 64, "bf16", True),
+    (1, 1, 1, 1, 1, 64, "bf16", False),
+    (1, 1, 1, 1, 700, 128, "bf16", True),        # one query row sees every key
+    (1, 2, 1, 640, 384, 64, "bf16", False),      # Nq > Nk, non-causal
+    (1, 8, 2, 1000, 1000, 128, "bf16", True),
+    (1, 2, 2, 129, 129, 64, "f32", True),
+    (1, 3, 3, 70, 333, 128, "f32", False),
+    (2, 4, 2, 200, 200, 128, "f32", True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,dtype,causal", SMALL)
+def test_small_shapes(ost, B, Hq, Hkv, Nq, Nk, d, dtype, causal):
+    _check_full(ost, Workload("small", "fwd", B, Hq, Hkv, Nq, Nk, d, dtype, causal, seed=Nq + Nk))
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_peaked_rows(ost, d, causal):
+    w = Workload("peaked", "fwd", 1, 2, 2, 384, 384, d, "bf16", causal, seed=11)
+    x, o, lse, scale = _run(ost, w, scale=8.0 * w.scale)
+    o_ref, lse_ref = oracle.attention_fwd(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), scale,
+                                          causal)
+    err = np.max(np.abs(to_f64(o) - o_ref))
+    assert err <= 2e-2
+    assert err <= 1e-2 * np.max(np.abs(o_ref))
+    assert np.max(np.abs(to_f64(lse) - lse_ref)) <= 1e-3
+
+
+def test_lse_optional(ost):
+    w = Workload("nolse", "fwd", 1, 2, 2, 200, 200, 64, "bf16", True, seed=5)
+    x, o, lse, scale = _run(ost, w, with_lse=False)
+    assert lse is None
+    o_ref, _ = oracle.attention_fwd(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), scale, True)
+    assert np.max(np.abs(to_f64(o) - o_ref)) <= 2e-2
+
+
+def test_mha_workload_full(ost):
+    """B=4, H=16, N=2048, d=64 bf16, every output element."""
+    _check_full(ost, WORKLOADS["fwd_mha_n2048_d64"])
+
+
+def test_causal_long_workload_sampled(ost):
+    """B=2, H=32, N=8192, d=128 causal bf16 at full size; the oracle computes
+    sampled rows one by one (each row is independent)."""
+    w = WORKLOADS["fwd_causal_n8192_d128"]
+    x, o, lse, scale = _run(ost, w)
+    q, k, v = to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"])
+    o, lse = to_f64(o), to_f64(lse)
+    rng = np.random.default_rng(0)
+    fixed = [0, 1, 127, 128, 129, 255, 4095, 4096, 8063, 8064, 8190, 8191]
+    for b, h in [(0, 0), (1, 31), (0, 17), (1, 5)]:
+        rows = np.unique(np.concatenate([fixed, rng.integers(0, w.Nq, 20)]))
+        o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, scale, True, b, h, rows)
+        assert np.max(np.abs(o[b, h, rows] - o_ref)) <= 2e-2
+        assert np.max(np.abs(lse[b, h, rows] - lse_ref)) <= 1e-3
