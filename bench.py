@@ -1,0 +1,470 @@
+"""Benchmark of the tiled-attention hot path on GB300.
+
+Default workload (N=1): the batched multi-head forward B=4, H=16, N=2048,
+d=64, bf16, non-causal. ``--workload`` selects the other workloads
+(fwd_causal_n8192_d128, bwd_causal_n4096_d128, decode_gqa_l4096,
+fwd_f32_single_head). A step is one pass of the workload's hot path through
+the C ABI on inputs already resident in HBM; L2 is flushed (256 MiB write)
+between timed steps unless the inputs exceed L2.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the float64 CPU
+oracle as the reference arm instead.
+
+Multi-GPU: every rank runs an independent replica of the workload (the path
+shards over batch and heads with no exchange), so value = N x units / max
+over ranks of the timed region ("scaling": "weak").
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20
+
+
+# ----------------------------------------------------------------- workload math
+
+def algorithmic_units(w):
+    """(per-step units, unit name, bound) for a workload.
+
+    FLOPs: 2 per multiply-add; the forward has two GEMMs (4·Nq·Nk·d per head,
+    causal counts only the visible pairs), the backward five (2.5x the
+    forward). Decode bytes: K and V read once plus q and o."""
+    if w.kind == "decode":
+        bytes_ = 2 * w.B * w.Hkv * w.Nk * w.d * 2 + 2 * w.B * w.Hq * w.d * 2
+        return bytes_, "GB/s", "hbm"
+    if w.causal:
+        shift = w.Nk - w.Nq
+        pairs = sum(min(w.Nk, i + shift + 1) for i in range(w.Nq))
+    else:
+        pairs = w.Nq * w.Nk
+    flops = 4.0 * w.B * w.Hq * w.d * pairs
+    if w.kind == "bwd":
+        flops *= 2.5
+    return flops, "TFLOP/s", "tensor"
+
+
+def rate(units, seconds, unit):
+    return units / seconds / (1e12 if unit == "TFLOP/s" else 1e9)
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 50 ms; the samples whose timestamps fall in
+    the timed window (or, for a window shorter than the period, the ones
+    next to it) give the reported clocks."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.t_start = self.t_end = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    @staticmethod
+    def _ts(text):
+        from datetime import datetime
+        try:
+            return datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            ts = self._ts(parts[0])
+            if ts is not None:
+                rows.append((ts, parts))
+        if not rows:
+            return None
+        sel = [p for ts, p in rows if self.t_start <= ts <= self.t_end]
+        if not sel:  # window shorter than the sampling period: nearest samples
+            before = [p for ts, p in rows if ts < self.t_start][-1:]
+            after = [p for ts, p in rows if ts > self.t_end][:1]
+            sel = before + after
+        num = lambda v: float(v) if v.replace(".", "", 1).isdigit() else None
+        sm = [num(p[1]) for p in sel if num(p[1]) is not None]
+        smax = [num(p[2]) for p in sel if num(p[2]) is not None]
+        reasons = set()
+        for p in sel:
+            for name, val in zip(self.REASONS, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sel)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(w, inputs, budget_s: float):
+    """Time the float64 oracle on whole (b, h) heads of the workload until the
+    budget is spent; returns (units processed, seconds, description)."""
+    import numpy as np
+    import oracle
+    from workloads import to_f64
+
+    units_total, _, _ = algorithmic_units(w)
+    t0 = time.perf_counter()
+    done = 0
+    if w.kind == "decode":
+        per_req = units_total / w.B
+        for b in range(w.B):
+            q = to_f64(inputs["q"][b:b + 1])
+            k, v = to_f64(inputs["k"][b:b + 1]), to_f64(inputs["v"][b:b + 1])
+            oracle.decode_splitkv(q, k, v, w.scale, w.num_splits)
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return per_req * done, time.perf_counter() - t0, f"{done} of {w.B} requests"
+    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    per_head = units_total / len(heads)
+    r = w.Hq // w.Hkv
+    for b, h in heads:
+        sl = lambda t, hh: to_f64(t[b:b + 1, hh:hh + 1])
+        q, k, v = sl(inputs["q"], h), sl(inputs["k"], h // r), sl(inputs["v"], h // r)
+        if w.kind == "bwd":
+            oracle.attention_bwd(q, k, v, sl(inputs["do"], h), w.scale, w.causal)
+        else:
+            oracle.attention_fwd(q, k, v, w.scale, w.causal)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return per_head * done, time.perf_counter() - t0, f"{done} of {len(heads)} heads (b, h)"
+
+
+def input_bytes(inputs):
+    return sum(t.numel() * t.element_size() for t in inputs.values())
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from workloads import make_inputs
+    units, unit, _ = algorithmic_units(w)
+    inputs = make_inputs(w)
+    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, inputs, budget / 4)
+    done_units, secs = 0.0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        u, s, desc = cpu_oracle_sample(w, inputs, budget)
+        done_units += u
+        secs += s
+    value = rate(done_units, secs, unit)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, flushed=input_bytes(inputs) < L2_BYTES),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": host_cores(), "kind": "oracle",
+                         "sample": f"per step {desc} of one batch, float64 NumPy"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+METRIC = "attn fwd/bwd TFLOP/s vs GB300 BF16 peak; split-KV decode GB/s vs HBM"
+
+
+def workload_config(w, flushed: bool):
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk,
+           "d": w.d, "causal": w.causal, "dtype": w.dtype}
+    if w.kind == "decode":
+        cfg["num_splits"] = w.num_splits
+    cfg["l2"] = ("flushed between timed steps (256 MiB write)" if flushed
+                 else "inputs larger than L2 (129 MB); no flush")
+    return cfg
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p.get("hbm_gbs"), p.get("bf16_tflops"), p.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+KERNEL_SOURCES = {"fwd": "fwd_tc.cu", "bwd": "bwd_tc.cu", "decode": "decode.cu"}
+FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def kernel_label(w):
+    if w.kind == "fwd":
+        return ("fwd_simt_kernel" if w.dtype == "f32" else "fwd_tc_kernel") + \
+            " (whole attn_fwd call, one launch)"
+    if w.kind == "bwd":
+        return "attn_bwd call (row-term preprocess + main kernel + dQ convert)"
+    return "attn_decode_splitkv call (split kernel + merge kernel)"
+
+
+def kernel_source_sha(kind):
+    import hashlib
+    path = os.path.join(ROOT, "online_softmax_tiled_gb300", "csrc", KERNEL_SOURCES[kind])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(w):
+    """Per-launch DRAM bytes (read + write) of the dominant kernel, from the
+    committed ncu summary profiles/traffic.json; null when the kernel source
+    changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entry = json.load(f).get(w.name)
+    if not entry or entry.get("source_sha") != kernel_source_sha(w.kind):
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import online_softmax_tiled_gb300 as ost
+    from workloads import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    ost.lib()
+    stream = torch.cuda.current_stream(dev)
+
+    host = make_inputs(w)
+    x = {k: t.to(dev) for k, t in host.items()}
+    units, unit, bound = algorithmic_units(w)
+    in_bytes = sum(t.numel() * t.element_size() for t in host.values())
+    flush = in_bytes < L2_BYTES
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    # --- one step of the hot path, device-resident inputs
+    if w.kind == "fwd":
+        o = torch.empty_like(x["q"])
+        lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
+        step = lambda: ost.attn_fwd(x["q"], x["k"], x["v"], o, lse, w.scale, w.causal, stream)
+        launches_per_step = 1
+        outs = (o, lse)
+    elif w.kind == "bwd":
+        o, lse = ost.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale)
+        ws = torch.empty(ost.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d),
+                         dtype=torch.uint8, device=dev)
+        dq, dk, dv = (torch.empty_like(x[n]) for n in ("q", "k", "v"))
+        step = lambda: ost.attn_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, dq, dk, dv,
+                                    w.scale, w.causal, ws, stream)
+        launches_per_step = 3
+        outs = (dq, dk, dv)
+    else:
+        ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq, w.d, w.num_splits),
+                         dtype=torch.uint8, device=dev)
+        o = torch.empty_like(x["q"])
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        step = lambda: ost.attn_decode_splitkv(x["q"], x["k"], x["v"], o, lse, w.scale,
+                                               w.num_splits, ws, stream)
+        launches_per_step = 2
+        outs = (o, lse)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        if flush:
+            flush_buf.fill_(1)
+        step()
+    assert ost.attn_sync_status(stream) == ost.ATTN_OK
+
+    if args.profile:
+        # Short run for ncu: warm-up plus `steps` launches, nothing else.
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize(dev)
+        assert ost.attn_sync_status(stream) == ost.ATTN_OK
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if sampler:
+        # bring clocks up before the timed region
+        t_end = time.time() + 0.5
+        while time.time() < t_end:
+            step()
+        torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    if sampler:
+        sampler.mark_start()
+    for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(i & 0xff)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    barrier()
+    if sampler:
+        sampler.mark_end()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert ost.attn_sync_status(stream) == ost.ATTN_OK
+
+    # --- end to end through the public API: pinned host inputs in, results out
+    host_pinned = {k: t.pin_memory() for k, t in host.items()}
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_pinned.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+    def e2e_step():
+        for k_, t in host_pinned.items():
+            x[k_].copy_(t, non_blocking=True)
+        step()
+        for dst, src in zip(out_host, outs):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 20))
+    barrier()
+    e_s.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e_e.record(stream)
+    barrier()
+    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    clocks = sampler.stop() if sampler else None
+
+    if rank == 0:
+        ms_per_step = total_ms / args.steps
+        value = rate(world * units * args.steps, total_ms / 1e3, unit)
+        hbm, tf_burst, tf_sust, src = load_peaks()
+        peak = hbm if bound == "hbm" else tf_burst
+        peak_source = f"{src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops burst'})"
+        if w.dtype == "f32":
+            # float32 FFMA path: 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz max clock
+            bound, peak, peak_source = "alu", FP32_FFMA_PEAK_TFLOPS, "derived (FFMA lanes x clock)"
+        achieved = rate(units, ms_per_step / 1e3, unit)
+        cpu_units, cpu_s, cpu_desc = cpu_oracle_sample(w, host, args.cpu_budget)
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, flush),
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": unit, "frac": achieved / peak,
+                         "peak_source": peak_source,
+                         "traffic": profiled_traffic(w),
+                         "kernel": kernel_label(w)},
+            "cpu_baseline": {"value": rate(cpu_units, cpu_s, unit), "unit": unit,
+                             "cores": host_cores(), "kind": "oracle",
+                             "sample": f"{cpu_desc} of one step, float64 NumPy, {cpu_s:.1f} s"},
+            "e2e": {"value": rate(world * units, e2e_ms / 1e3, unit), "unit": unit,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    from workloads import WORKLOADS
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="fwd_mha_n2048_d64", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of CPU oracle work for the cpu_baseline figure")
+    ap.add_argument("--profile", action="store_true",
+                    help="only warm-up and timed launches, no JSON line (for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
