@@ -158,6 +158,40 @@ ATTN_API attn_status attn_merge_partials(const float* o_part, const float* m_par
                                 void* o, float* lse, int rows, int num_splits, int d,
                                 attn_dtype out_dt, void* stream);
 
+/*
+ * Split-KV decode without any allocation by the caller.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory at the point where they decode — for
+ * example a serving loop whose memory is partitioned up front and that must
+ * not call cudaMalloc after start-up (cudaMalloc can synchronise the device
+ * and its latency is unpredictable), or a plugin inside a host program that
+ * owns all device memory and exposes no allocator. It computes exactly what
+ * attn_decode_splitkv computes, with the same arguments minus the workspace.
+ *
+ * Scratch: the per-split partials live in one fixed array inside the library
+ * of ATTN_DECODE_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the
+ * library holds until the process exits. A call whose partials need more
+ * than that (attn_decode_workspace_size(B, Hq, d, num_splits) larger than
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES) is rejected with ATTN_ERR_WORKSPACE and
+ * nothing is launched.
+ *
+ * Set-up: the first call on a device looks up that device's address of the
+ * array (cudaGetSymbolAddress, with the device current) and caches it; make
+ * that first call before any stream capture on the device.
+ *
+ * Sharing: all calls on a device use the same array. Nothing in it needs to
+ * start at zero (each call writes every partial it reads), but calls whose
+ * kernels overlap on the GPU (different streams without ordering between
+ * them) race on the array and give wrong results; order them on one stream.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+
+ATTN_API attn_status attn_decode_splitkv_noalloc(const void* q, const void* k_cache,
+                                                 const void* v_cache, void* o, float* lse, int B,
+                                                 int Hq, int Hkv, int L, int d, float scale,
+                                                 int num_splits, void* stream);
+
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status s);
 

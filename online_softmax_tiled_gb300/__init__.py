@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_workspace_size,
     attn_decode_splitkv,
+    attn_decode_splitkv_noalloc,
     attn_decode_workspace_size,
     attn_fwd,
     attn_merge_partials,

@@ -48,6 +48,8 @@ _SIGNATURES = {
                              ctypes.c_void_p]),
     "attn_merge_partials": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
                             [ctypes.c_void_p]),
+    "attn_decode_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 +
+                                    [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
 }
@@ -148,6 +150,20 @@ def attn_decode_splitkv(q, k_cache, v_cache, o, lse, scale: float, num_splits: i
                                    Hq, Hkv, L, d, float(scale), int(num_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "attn_decode_splitkv")
+
+
+def attn_decode_splitkv_noalloc(q, k_cache, v_cache, o, lse, scale: float, num_splits: int,
+                                stream=None):
+    """Split-KV decode whose partials live in the library's fixed scratch array
+    (no workspace argument): for callers that cannot allocate device memory
+    when they decode. Same shapes and results as attn_decode_splitkv."""
+    _device_contig(q, k_cache, v_cache, o, lse)
+    B, Hq, d = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    st = lib().attn_decode_splitkv_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o),
+                                           _ptr(lse), B, Hq, Hkv, L, d, float(scale),
+                                           int(num_splits), _stream(stream))
+    _check(st, "attn_decode_splitkv_noalloc")
 
 
 def attn_merge_partials(o_part, m_part, l_part, o, lse, stream=None):

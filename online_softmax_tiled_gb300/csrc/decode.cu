@@ -21,6 +21,8 @@
 // group runs its own online softmax over its keys; the 16 groups of the CTA
 // are merged with the same exact rule at the end.
 
+#include <mutex>
+
 #include "common.cuh"
 #include "launchers.h"
 
@@ -339,6 +341,52 @@ cudaError_t launch_merge(const MergeArgs& a) {
         a.o_part, a.m_part, a.l_part, static_cast<__nv_bfloat16*>(a.o), a.lse, a.rows,
         a.num_splits, a.d);
   return cudaGetLastError();
+}
+
+}  // namespace attn
+
+// ----------------------------------------------------------------------------
+// attn_decode_splitkv_noalloc: the same decode, with the split partials kept
+// in a fixed array inside the library instead of a caller workspace, for
+// callers that cannot allocate device memory when they decode.
+// ----------------------------------------------------------------------------
+namespace attn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = ATTN_DECODE_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};  // device address of the array, per device
+
+}  // namespace
+
+extern "C" ATTN_API attn_status attn_decode_splitkv_noalloc(const void* q, const void* k_cache,
+                                                            const void* v_cache, void* o,
+                                                            float* lse, int B, int Hq, int Hkv,
+                                                            int L, int d, float scale,
+                                                            int num_splits, void* stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    // Once per device, with that device current: the host-side name of the
+    // array is not a device address, so ask the runtime for this device's.
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_decode_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return ATTN_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // The workspace path validates every argument, rejects a call whose
+  // partials exceed the array (ATTN_ERR_WORKSPACE) and launches nothing then.
+  return attn_decode_splitkv(q, k_cache, v_cache, o, lse, B, Hq, Hkv, L, d, scale, num_splits,
+                             scratch, kNoAllocScratchBytes, stream);
 }
 
 }  // namespace attn
