@@ -1,8 +1,539 @@
-// bf16 backward entry (tcgen05 kernel under construction; routes to the FFMA kernel).
+// bf16 attention backward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Recomputation backward of the "Flash Attention 2" post
+// (ahmadsaeedzaidi.github.io feed), section "Flash Attention 2",
+// "Recomputation in backward pass": nothing N×N is stored by the forward; S
+// and P are rebuilt tile by tile, P = exp(scale·S - LSE) from the saved row
+// LSE. The softmax step is the Jacobian-vector product of the
+// softmax-backward note (shreyansh26.github.io feed), section
+// "Backpropagating Through Softmax": dS = P ∘ (dP - D) with dP = dO Vᵀ and
+// the row term D = rowsum(dO ∘ O) (preprocess kernel). Then dV = Pᵀ dO,
+// dK = scale·dSᵀ Q, dQ = scale·dS K.
+//
+// GB300 mapping:
+//  * One CTA owns a 128-key tile K_j, V_j of one KV head (K-major in shared
+//    memory, loaded once by TMA) and loops over every query head of its GQA
+//    group and every query tile Q_i, dO_i (BQ rows) that sees those keys.
+//  * Per step, with keys on the 128 TMEM lanes:
+//      Sᵀ = K_j Q_iᵀ and dPᵀ = V_j dO_iᵀ          (tcgen05.mma, fp32 in TMEM)
+//      Pᵀ = exp2(Sᵀ·scale·log2e - LSE·log2e), dSᵀ = Pᵀ ∘ (dPᵀ - D)
+//                                     (one warpgroup, one key row per thread,
+//                                      bf16 into swizzled shared memory)
+//      dV_j += Pᵀ dO_i, dK_j += dSᵀ Q_i           (TMEM accumulators, d columns)
+//      dQ_i  = dS K_j                             (TMEM; for d = 128 computed
+//                                      transposed, dQᵀ = K_jᵀ dSᵀ, so that
+//                                      M = 128)
+//    The next step's Sᵀ, dPᵀ are issued before this step's dV, dK, dQ so the
+//    softmax of step s+1 overlaps the tensor core's work of step s.
+//  * dQ has many writers (every key tile of the head); a third warpgroup
+//    drains each dQ tile from TMEM and adds it (scaled) into the float32
+//    accumulator with coalesced reductions; the attention-residuals lab
+//    (manishklach.github.io) reduces multi-writer gradients the same way.
+//    dK and dV have one writer: the CTA stores them once, by TMA.
+//  * Every mbarrier wait is bounded (error word + abort flag + drain).
+
 #include "common.cuh"
 #include "launchers.h"
+#include "tc_ptx.cuh"
+#include "tma_host.h"
 
 namespace attn {
+
 ATTN_DEFINE_ERROR_WORD(take_error_bwd_tc)
-cudaError_t launch_bwd_tc(const BwdArgs& a) { return launch_bwd_simt(a); }
+
+namespace {
+
+constexpr int kBK = 128;            // keys per CTA (TMEM lanes)
+constexpr int kThreads = 384;       // 12 warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BQ = (D == 128) ? 64 : 128;        // query rows per step
+  static constexpr bool kDqTransposed = (D == 128);       // dQᵀ (M = d) vs dQ (M = BQ)
+  static constexpr int kPsBufs = (D == 128) ? 2 : 1;      // Pᵀ/dSᵀ shared-memory buffers
+  static constexpr int kQStages = 2;
+  // shared memory (bytes; every tile 1024-aligned)
+  static constexpr int kKVTile = kBK * D * 2;             // K_j or V_j
+  static constexpr int kQTile = BQ * D * 2;               // Q_i or dO_i
+  static constexpr int kPsTile = kBK * BQ * 2;            // Pᵀ or dSᵀ
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kKVTile;
+  static constexpr int kOffQ = kOffV + kKVTile;                      // [stage] Q, dO
+  static constexpr int kOffP = kOffQ + kQStages * 2 * kQTile;       // [buf] Pᵀ, dSᵀ
+  static constexpr int kOffVec = kOffP + kPsBufs * 2 * kPsTile;     // [stage] LSE2, D
+  static constexpr int kSmemBytes = kOffVec + kQStages * 2 * BQ * 4;
+  static constexpr int kDynSmem = kSmemBytes + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = BQ;
+  static constexpr uint32_t kColDQ = 2 * BQ;                         // 2 buffers
+  static constexpr uint32_t kDqCols = kDqTransposed ? BQ : D;
+  static constexpr uint32_t kColDV = kColDQ + 2 * kDqCols;
+  static constexpr uint32_t kColDK = kColDV + D;
+  static_assert(kColDK + D <= 512, "TMEM budget");
+  static_assert(kDynSmem <= 232448, "shared-memory budget");
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t sdp_full, p_full;
+  uint64_t ps_free[2];
+  uint64_t dq_full[2], dq_free[2];
+  uint64_t dkv_full, mma_drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+ATTN_DEVINL void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
+                              int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+ATTN_DEVINL void tma_store_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+ATTN_DEVINL void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+ATTN_DEVINL void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d) : "memory");
+}
+
+// Byte offset of element (row, col) of a bf16 tile stored as 64-column,
+// 128-byte-swizzled atoms of `rows` rows each (the TMA SWIZZLE_128B layout).
+ATTN_DEVINL uint32_t sw128_offset(int row, int col, int rows) {
+  const int atom = col >> 6, c = col & 63;
+  const int chunk = c >> 3;
+  return uint32_t(atom * rows * 128 + row * 128 + ((chunk ^ (row & 7)) << 4) + ((c & 7) << 1));
+}
+
+// The (head, query tile) steps of one CTA: every query head of the group,
+// query tiles from the first one that sees key k0 (causal) to the last.
+struct StepPlan {
+  int first_tile, tiles_per_head, group, n;
+  ATTN_DEVINL void init(int k0, int Nq, int Nk, int causal, int group_, int BQ) {
+    group = group_;
+    const int nq_tiles = (Nq + BQ - 1) / BQ;
+    first_tile = 0;
+    if (causal) first_tile = max(0, k0 - (Nk - Nq)) / BQ;
+    tiles_per_head = max(0, nq_tiles - first_tile);
+    n = (k0 < Nk) ? tiles_per_head * group : 0;
+  }
+  ATTN_DEVINL void at(int s, int& hh, int& qt) const {
+    hh = s / tiles_per_head;
+    qt = first_tile + s % tiles_per_head;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+              const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
+              const float* __restrict__ lse, const float* __restrict__ row_term,
+              float* __restrict__ dq_acc, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
+              int n_ktiles) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ BwdBars bars;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Key tiles in ascending order across all heads: the tiles with the most
+  // query steps (causal) start first.
+  const int n_bhkv = int(gridDim.x) / n_ktiles;
+  const int ktile = int(blockIdx.x) / n_bhkv;
+  const int bhkv = int(blockIdx.x) % n_bhkv;
+  const int b = bhkv / Hkv, g = bhkv % Hkv;
+  const int group = Hq / Hkv;
+  const int k0 = ktile * kBK;
+  StepPlan plan;
+  plan.init(k0, Nq, Nk, causal, group, BQ);
+  const int n = plan.n;
+
+  if (tid == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.q_full[i], 1 + 32);   // TMA producer + 32 LSE/D loader lanes
+      mbar_init(&bars.q_empty[i], 1);
+      mbar_init(&bars.ps_free[i], 1);
+      mbar_init(&bars.dq_full[i], 1);
+      mbar_init(&bars.dq_free[i], 128);
+    }
+    mbar_init(&bars.sdp_full, 1);
+    mbar_init(&bars.p_full, 128);
+    mbar_init(&bars.dkv_full, 1);
+    mbar_init(&bars.mma_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars.tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0 && n > 0) {
+      tc::tma_prefetch_desc(&map_q);
+      tc::tma_prefetch_desc(&map_do);
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * C::kKVTile);
+      for (int a = 0; a < D / 64; ++a) {
+        tc::tma_load_3d(smem + C::kOffK + a * kBK * 128, &map_k, 64 * a, k0, bhkv, &bars.kv_full);
+        tc::tma_load_3d(smem + C::kOffV + a * kBK * 128, &map_v, 64 * a, k0, bhkv, &bars.kv_full);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int s = 0; s < n && ok; ++s) {
+        const int st = s & 1;
+        if (s >= 2) ok = mbar_wait_bounded(&bars.q_empty[st], ((s >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        int hh, qt;
+        plan.at(s, hh, qt);
+        const int bh = b * Hq + g * group + hh;
+        mbar_arrive_expect_tx(&bars.q_full[st], 2 * C::kQTile);
+        uint8_t* qs = smem + C::kOffQ + st * 2 * C::kQTile;
+        for (int a = 0; a < D / 64; ++a) {
+          tc::tma_load_3d(qs + a * BQ * 128, &map_q, 64 * a, qt * BQ, bh, &bars.q_full[st]);
+          tc::tma_load_3d(qs + C::kQTile + a * BQ * 128, &map_do, 64 * a, qt * BQ, bh,
+                          &bars.q_full[st]);
+        }
+        ++issued;
+      }
+      if (!ok) {
+        attn_flag_error(kErrTimeout);
+        bars.abort = 1;
+        mbar_wait_bounded(&bars.kv_full, 0, nullptr);
+        for (int s = max(0, issued - 2); s < issued; ++s)
+          mbar_wait_bounded(&bars.q_full[s & 1], (s >> 1) & 1, nullptr);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- LSE / D loader
+    // Per step: LSE·log2e and D of the BQ query rows into the stage's vectors;
+    // rows past Nq get LSE = +inf (P = 0) and D = 0.
+    bool ok = true;
+    for (int s = 0; s < n && ok; ++s) {
+      const int st = s & 1;
+      if (s >= 2)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(&bars.q_empty[st], ((s >> 1) - 1) & 1, abort_flag));
+      if (!ok) break;
+      int hh, qt;
+      plan.at(s, hh, qt);
+      const size_t bh = size_t(b) * Hq + g * group + hh;
+      float* vec = reinterpret_cast<float*>(smem + C::kOffVec + st * 2 * BQ * 4);
+      for (int c = lane; c < BQ; c += 32) {
+        const int q = qt * BQ + c;
+        const bool in = q < Nq;
+        vec[c] = in ? lse[bh * Nq + q] * kLog2e : INFINITY;
+        vec[BQ + c] = in ? row_term[bh * Nq + q] : 0.f;
+      }
+      mbar_arrive(&bars.q_full[st]);
+    }
+    if (!ok && lane == 0) {
+      attn_flag_error(kErrTimeout);
+      bars.abort = 1;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_sdp = tc::idesc_bf16_f32(kBK, BQ, false, false);
+      constexpr uint32_t idesc_kv = tc::idesc_bf16_f32(kBK, D, false, true);
+      constexpr uint32_t idesc_dq = C::kDqTransposed ? tc::idesc_bf16_f32(D, BQ, true, true)
+                                                     : tc::idesc_bf16_f32(BQ, D, true, true);
+      const uint32_t k_s = smem_u32(smem + C::kOffK);
+      const uint32_t v_s = smem_u32(smem + C::kOffV);
+      bool ok = true;
+
+      auto issue_sdp = [&](int s) {   // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
+        const uint32_t qa = smem_u32(smem + C::kOffQ + (s & 1) * 2 * C::kQTile);
+        const uint32_t da = qa + C::kQTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // K_j / V_j K-major
+          const uint32_t qb = (kk / 4) * (BQ * 128) + (kk % 4) * 32;    // Q_i / dO_i K-major
+          tc::mma_ss(tmem + C::kColS, tc::smem_desc(k_s + ka, 16, 1024, tc::kLayoutSW128),
+                     tc::smem_desc(qa + qb, 16, 1024, tc::kLayoutSW128), idesc_sdp, kk > 0);
+          tc::mma_ss(tmem + C::kColDP, tc::smem_desc(v_s + ka, 16, 1024, tc::kLayoutSW128),
+                     tc::smem_desc(da + qb, 16, 1024, tc::kLayoutSW128), idesc_sdp, kk > 0);
+        }
+        tc::mma_commit(&bars.sdp_full);
+      };
+
+      if (n > 0) {
+        ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
+        if (ok) ok = mbar_wait_bounded(&bars.q_full[0], 0, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_sdp(0);
+        }
+      }
+      for (int s = 0; s < n && ok; ++s) {
+        const int st = s & 1;
+        const int pb = s % C::kPsBufs;
+        ok = mbar_wait_bounded(&bars.p_full, s & 1, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        if (s + 1 < n) {
+          ok = mbar_wait_bounded(&bars.q_full[(s + 1) & 1], ((s + 1) >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_sdp(s + 1);
+        }
+        const uint32_t qa = smem_u32(smem + C::kOffQ + st * 2 * C::kQTile);
+        const uint32_t da = qa + C::kQTile;
+        const uint32_t pa = smem_u32(smem + C::kOffP + pb * 2 * C::kPsTile);
+        const uint32_t sa = pa + C::kPsTile;
+        // dV += Pᵀ dO ; dK += dSᵀ Q   (M = keys, N = d, K = BQ queries)
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t pk = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // Pᵀ/dSᵀ K-major
+          const uint32_t qm = kk * 2048;                                  // dO/Q MN-major
+          const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+          tc::mma_ss(tmem + C::kColDV, tc::smem_desc(pa + pk, 16, 1024, tc::kLayoutSW128),
+                     tc::smem_desc(da + qm, BQ * 128, 1024, tc::kLayoutSW128), idesc_kv, acc);
+          tc::mma_ss(tmem + C::kColDK, tc::smem_desc(sa + pk, 16, 1024, tc::kLayoutSW128),
+                     tc::smem_desc(qa + qm, BQ * 128, 1024, tc::kLayoutSW128), idesc_kv, acc);
+        }
+        tc::mma_commit(&bars.q_empty[st]);
+        // dQ (or dQᵀ) into TMEM buffer s & 1, once the drain of step s-2 freed it.
+        if (s >= 2) {
+          ok = mbar_wait_bounded(&bars.dq_free[st], ((s >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+        }
+        const uint32_t dq_col = C::kColDQ + st * C::kDqCols;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t km = kk * 2048;   // 16 keys down both MN-major operands
+          if (C::kDqTransposed)   // dQᵀ = K_jᵀ dSᵀ: A = K_j (MN-major, d atoms), B = dSᵀ
+            tc::mma_ss(tmem + dq_col, tc::smem_desc(k_s + km, kBK * 128, 1024, tc::kLayoutSW128),
+                       tc::smem_desc(sa + km, kBK * 128, 1024, tc::kLayoutSW128), idesc_dq, kk > 0);
+          else                    // dQ = dS K_j: A = dSᵀ (MN-major, query atoms), B = K_j
+            tc::mma_ss(tmem + dq_col, tc::smem_desc(sa + km, kBK * 128, 1024, tc::kLayoutSW128),
+                       tc::smem_desc(k_s + km, kBK * 128, 1024, tc::kLayoutSW128), idesc_dq, kk > 0);
+        }
+        tc::mma_commit(&bars.dq_full[st]);
+        tc::mma_commit(&bars.ps_free[pb]);
+      }
+      if (!ok) {
+        attn_flag_error(kErrTimeout);
+        bars.abort = 1;
+      }
+      tc::mma_commit(&bars.dkv_full);
+      tc::mma_commit(&bars.mma_drain);
+      mbar_wait_bounded(&bars.mma_drain, 0, nullptr);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroup
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // key row in the tile (TMEM lane)
+    const int key = k0 + r;
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const float c = scale * kLog2e;
+    const int shift = Nk - Nq;
+    bool ok = true;
+    for (int s = 0; s < n; ++s) {
+      const int st = s & 1;
+      const int pb = s % C::kPsBufs;
+      int hh, qt;
+      plan.at(s, hh, qt);
+      const int q0 = qt * BQ;
+      bool w = mbar_wait_bounded(&bars.sdp_full, s & 1, abort_flag);
+      w = w && mbar_wait_bounded(&bars.q_full[st], (s >> 1) & 1, abort_flag);
+      if (s >= C::kPsBufs)
+        w = w && mbar_wait_bounded(&bars.ps_free[pb], ((s / C::kPsBufs) - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc::fence_after_sync();
+      const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * BQ * 4);
+      uint8_t* pt = smem + C::kOffP + pb * 2 * C::kPsTile;
+      uint8_t* dst = pt + C::kPsTile;
+      const bool key_in = key < Nk;
+      // first visible query column of this key row (causal), relative to q0
+      const int qmin = causal ? key - shift - q0 : -1;
+#pragma unroll
+      for (int half = 0; half < BQ / 32; ++half) {
+        uint32_t sr[32], dr[32];
+        tc::tmem_ld32(tmem + lane_base + C::kColS + half * 32, sr);
+        tc::tmem_ld32(tmem + lane_base + C::kColDP + half * 32, dr);
+        tc::tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = half * 32 + 2 * e + u;
+            const float l2 = vec[col];
+            float p = fast_exp2(fmaf(__uint_as_float(sr[2 * e + u]), c, -l2));
+            if (!key_in || col < qmin) p = 0.f;
+            pv[u] = p;
+            dv[u] = p * (__uint_as_float(dr[2 * e + u]) - vec[BQ + col]);
+          }
+          pk[e] = pack_bf16x2(pv[0], pv[1]);
+          dk[e] = pack_bf16x2(dv[0], dv[1]);
+        }
+        // 32 columns = 4 chunks of 16 bytes in row r
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t off = sw128_offset(r, half * 32 + u * 8, kBK);
+          *reinterpret_cast<uint4*>(pt + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          *reinterpret_cast<uint4*>(dst + off) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();      // generic-proxy writes -> tensor-core (async proxy) reads
+      tc::fence_before_sync();
+      mbar_arrive(&bars.p_full);
+    }
+    if (!ok) {
+      if (lane == 0) attn_flag_error(kErrTimeout);
+      bars.abort = 1;
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------- dQ drain, dK/dV epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                 // TMEM lane
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    bool ok = true;
+    for (int s = 0; s < n; ++s) {
+      const int st = s & 1;
+      int hh, qt;
+      plan.at(s, hh, qt);
+      const size_t bh = size_t(b) * Hq + g * group + hh;
+      const int q0 = qt * BQ;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars.dq_full[st], (s >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t col0 = C::kColDQ + st * C::kDqCols;
+      uint32_t v0[32], v1[32];
+      tc::tmem_ld32(tmem + lane_base + col0, v0);
+      tc::tmem_ld32(tmem + lane_base + col0 + 32, v1);
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      mbar_arrive(&bars.dq_free[st]);
+      if (C::kDqTransposed) {
+        // lane r = dimension, columns = the BQ (= 64) query rows of the step
+        float* base = dq_acc + (bh * Nq + q0) * D + r;
+        const int nrows = min(BQ, Nq - q0);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          if (e < nrows) atomicAdd(base + size_t(e) * D, __uint_as_float(v0[e]) * scale);
+          if (e + 32 < nrows) atomicAdd(base + size_t(e + 32) * D, __uint_as_float(v1[e]) * scale);
+        }
+      } else {
+        // lane r = query row, columns = the d (= 64) dimensions
+        if (q0 + r < Nq) {
+          float* row = dq_acc + (bh * Nq + q0 + r) * D;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            red_add_v4(row + e, __uint_as_float(v0[e]) * scale, __uint_as_float(v0[e + 1]) * scale,
+                       __uint_as_float(v0[e + 2]) * scale, __uint_as_float(v0[e + 3]) * scale);
+            red_add_v4(row + 32 + e, __uint_as_float(v1[e]) * scale,
+                       __uint_as_float(v1[e + 1]) * scale, __uint_as_float(v1[e + 2]) * scale,
+                       __uint_as_float(v1[e + 3]) * scale);
+          }
+        }
+      }
+    }
+    // dK = scale·(dSᵀ Q summed), dV = Pᵀ dO summed -> bf16 -> K_j / V_j tiles -> TMA store.
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.dkv_full, 0, abort_flag));
+    if (ok) {
+      tc::fence_after_sync();
+      uint8_t* kst = smem + C::kOffK;
+      uint8_t* vst = smem + C::kOffV;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t kr[32], vr[32];
+        if (n > 0) {
+          tc::tmem_ld32(tmem + lane_base + C::kColDK + ch * 32, kr);
+          tc::tmem_ld32(tmem + lane_base + C::kColDV + ch * 32, vr);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) kr[e] = vr[e] = 0u;   // no query sees these keys
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t kp[4], vp[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = u * 8 + 2 * e;
+            kp[e] = pack_bf16x2(__uint_as_float(kr[i]) * scale, __uint_as_float(kr[i + 1]) * scale);
+            vp[e] = pack_bf16x2(__uint_as_float(vr[i]), __uint_as_float(vr[i + 1]));
+          }
+          const uint32_t off = sw128_offset(r, ch * 32 + u * 8, kBK);
+          *reinterpret_cast<uint4*>(kst + off) = make_uint4(kp[0], kp[1], kp[2], kp[3]);
+          *reinterpret_cast<uint4*>(vst + off) = make_uint4(vp[0], vp[1], vp[2], vp[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (quarter == 0 && lane == 0) {
+        for (int a = 0; a < D / 64; ++a) {
+          tma_store_3d(&map_dk, kst + a * kBK * 128, 64 * a, k0, bhkv);
+          tma_store_3d(&map_dv, vst + a * kBK * 128, 64 * a, k0, bhkv);
+        }
+        tma_store_commit_and_wait();
+      }
+    } else {
+      if (lane == 0) attn_flag_error(kErrTimeout);
+      bars.abort = 1;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
+  using C = BwdCfg<D>;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
+  const uint64_t bhq = uint64_t(a.B) * a.Hq, bhk = uint64_t(a.B) * a.Hkv;
+  if (!make_map_bf16_3d(&mq, a.q, D, a.Nq, bhq, C::BQ) ||
+      !make_map_bf16_3d(&mdo, a.dO, D, a.Nq, bhq, C::BQ) ||
+      !make_map_bf16_3d(&mk, a.k, D, a.Nk, bhk, kBK) ||
+      !make_map_bf16_3d(&mv, a.v, D, a.Nk, bhk, kBK) ||
+      !make_map_bf16_3d(&mdk, a.dk, D, a.Nk, bhk, kBK) ||
+      !make_map_bf16_3d(&mdv, a.dv, D, a.Nk, bhk, kBK))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+  if (e != cudaSuccess) return e;
+  const int n_ktiles = (a.Nk + kBK - 1) / kBK;
+  const long blocks = long(n_ktiles) * a.B * a.Hkv;
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
+      mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale,
+      a.causal, n_ktiles);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdArgs& a) {
+  return a.d == 64 ? launch_bwd_tc_d<64>(a) : launch_bwd_tc_d<128>(a);
+}
+
 }  // namespace attn
