@@ -121,10 +121,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __shared__ Bars bars;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Heaviest (latest) query blocks of every head first.
-  const int BH = gridDim.x / n_qblk;
-  const int qblk = n_qblk - 1 - int(blockIdx.x) / BH;
-  const int bh = int(blockIdx.x) % BH;
+  // Head-major order (a head's K/V stay in L2 while its query blocks run),
+  // heaviest (latest, for causal) query block of each head first.
+  const int bh = int(blockIdx.x) / n_qblk;
+  const int qblk = n_qblk - 1 - int(blockIdx.x) % n_qblk;
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int row0 = qblk * 2 * kBM;
@@ -158,8 +158,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
+  // Register split: 128 x 80 (TMA, MMA, idle warps) + 256 x 208 (softmax)
+  // <= 384 x 168 registers the CTA is launched with.
+  // Register split, set inside each role: 128 x 80 (TMA, MMA, idle warps) +
+  // 256 x 208 (softmax) <= 384 x 168 registers the CTA is launched with.
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    regs_dec<80>();
     if (lane == 0 && nj > 0) {
       tc::tma_prefetch_desc(&map_q);
       tc::tma_prefetch_desc(&map_k);
@@ -203,6 +209,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    regs_dec<80>();
     if (lane == 0 && nj > 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, false, true);
@@ -269,8 +276,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tc::mma_commit(&bars.mma_drain);
       mbar_wait_bounded(&bars.mma_drain, 0, nullptr);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 4) {
+    regs_dec<80>();                                // idle warps of the first warpgroup
+  } else {
     // ------------------------------------------------------------ softmax warpgroups
+    regs_inc<208>();
     const int t = (warp - 4) / 4;                  // query tile of this warpgroup
     const int quarter = warp % 4;                  // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;             // row within the tile (TMEM lane)
@@ -308,9 +318,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int cc = 0; cc < kBN; ++cc)
           if (key0 + cc > limit) s[cc] = -INFINITY;
       }
-      float mx = s[0];
+      float mx = max3(s[0], s[1], s[2]);
 #pragma unroll
-      for (int cc = 1; cc < kBN; ++cc) mx = fmaxf(mx, s[cc]);
+      for (int cc = 3; cc < kBN - 1; cc += 2) mx = max3(mx, s[cc], s[cc + 1]);
+      mx = fmaxf(mx, s[kBN - 1]);
       const float m_cand = fmaxf(m_ref, mx * c);
       const bool need = m_cand - m_ref > kRescaleThreshold;   // also true while m_ref = -inf
       float alpha = 1.f;
@@ -321,19 +332,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
       // P̃ = exp2(s·c - m_ref) -> bf16 pairs into the first 64 columns of S.
-      float rs = 0.f;
+      const f2 cc2{c, c}, nm2{neg_m, neg_m};
+      f2 rs2{0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = fast_exp2(fmaf(s[half * 64 + 2 * e], c, neg_m));
-          const float p1 = fast_exp2(fmaf(s[half * 64 + 2 * e + 1], c, neg_m));
-          rs += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          f2 x = fma2(f2{s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]}, cc2, nm2);
+          x.x = fast_exp2(x.x);
+          x.y = fast_exp2(x.y);
+          rs2 = add2(rs2, x);
+          pk[e] = pack_bf16x2(x.x, x.y);
         }
         tmem_st32(s_addr + half * 32, pk);
       }
+      const float rs = rs2.x + rs2.y;
       l_run = fmaf(alpha, l_run, rs);
 
       // Rescale Õ (once the previous P̃V has landed) when the reference moved.
