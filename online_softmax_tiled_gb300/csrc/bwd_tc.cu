@@ -185,8 +185,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
+  // Register split, set inside each role (launch: 384 x 168): warps 0-3
+  // (TMA, MMA, LSE/D loader, idle) 88; Pᵀ/dSᵀ warpgroup 216; dQ/epilogue
+  // warpgroup 200. 128 x (88 + 216 + 200) = 384 x 168.
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
+    regs_dec<88>();
     if (lane == 0 && n > 0) {
       tc::tma_prefetch_desc(&map_q);
       tc::tma_prefetch_desc(&map_do);
@@ -223,8 +227,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------- LSE / D loader
-    // Per step: LSE·log2e and D of the BQ query rows into the stage's vectors;
-    // rows past Nq get LSE = +inf (P = 0) and D = 0.
+    regs_dec<88>();
+    // Per step: -LSE·log2e and -D of the BQ query rows into the stage's
+    // vectors; rows past Nq get -LSE·log2e = -inf (P = 0) and -D = 0.
     bool ok = true;
     for (int s = 0; s < n && ok; ++s) {
       const int st = s & 1;
@@ -239,8 +244,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       for (int c = lane; c < BQ; c += 32) {
         const int q = qt * BQ + c;
         const bool in = q < Nq;
-        vec[c] = in ? lse[bh * Nq + q] * kLog2e : INFINITY;
-        vec[BQ + c] = in ? row_term[bh * Nq + q] : 0.f;
+        vec[c] = in ? -lse[bh * Nq + q] * kLog2e : -INFINITY;
+        vec[BQ + c] = in ? -row_term[bh * Nq + q] : 0.f;
       }
       mbar_arrive(&bars.q_full[st]);
     }
@@ -250,6 +255,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    regs_dec<88>();
     if (lane == 0) {
       constexpr uint32_t idesc_sdp = tc::idesc_bf16_f32(kBK, BQ, false, false);
       constexpr uint32_t idesc_kv = tc::idesc_bf16_f32(kBK, D, false, true);
@@ -259,13 +265,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const uint32_t v_s = smem_u32(smem + C::kOffV);
       bool ok = true;
 
-      auto issue_sdp = [&](int s) {   // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ
+      auto issue_sdp = [&](int s) {   // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ (all operands K-major)
         const uint32_t qa = smem_u32(smem + C::kOffQ + (s & 1) * 2 * C::kQTile);
         const uint32_t da = qa + C::kQTile;
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // K_j / V_j K-major
-          const uint32_t qb = (kk / 4) * (BQ * 128) + (kk % 4) * 32;    // Q_i / dO_i K-major
+          const uint32_t ka = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // K_j / V_j
+          const uint32_t qb = (kk / 4) * (BQ * 128) + (kk % 4) * 32;    // Q_i / dO_i
           tc::mma_ss(tmem + C::kColS, tc::smem_desc(k_s + ka, 16, 1024, tc::kLayoutSW128),
                      tc::smem_desc(qa + qb, 16, 1024, tc::kLayoutSW128), idesc_sdp, kk > 0);
           tc::mma_ss(tmem + C::kColDP, tc::smem_desc(v_s + ka, 16, 1024, tc::kLayoutSW128),
@@ -299,15 +305,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const uint32_t pa = smem_u32(smem + C::kOffP + pb * 2 * C::kPsTile);
         const uint32_t sa = pa + C::kPsTile;
         // dV += Pᵀ dO ; dK += dSᵀ Q   (M = keys, N = d, K = BQ queries)
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t pk = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // Pᵀ/dSᵀ K-major
-          const uint32_t qm = kk * 2048;                                  // dO/Q MN-major
-          const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-          tc::mma_ss(tmem + C::kColDV, tc::smem_desc(pa + pk, 16, 1024, tc::kLayoutSW128),
-                     tc::smem_desc(da + qm, BQ * 128, 1024, tc::kLayoutSW128), idesc_kv, acc);
-          tc::mma_ss(tmem + C::kColDK, tc::smem_desc(sa + pk, 16, 1024, tc::kLayoutSW128),
-                     tc::smem_desc(qa + qm, BQ * 128, 1024, tc::kLayoutSW128), idesc_kv, acc);
+        {
+          const uint64_t dv_b = tc::smem_desc(da, BQ * 128, 1024, tc::kLayoutSW128);  // dO MN-major
+          const uint64_t dk_b = tc::smem_desc(qa, BQ * 128, 1024, tc::kLayoutSW128);  // Q MN-major
+#pragma unroll 1
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint32_t pk = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // Pᵀ/dSᵀ K-major
+            const uint64_t step = uint64_t(kk * 2048) >> 4;               // 16 query rows down
+            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+            tc::mma_ss(tmem + C::kColDV, tc::smem_desc(pa + pk, 16, 1024, tc::kLayoutSW128),
+                       dv_b + step, idesc_kv, acc);
+            tc::mma_ss(tmem + C::kColDK, tc::smem_desc(sa + pk, 16, 1024, tc::kLayoutSW128),
+                       dk_b + step, idesc_kv, acc);
+          }
         }
         tc::mma_commit(&bars.q_empty[st]);
         // dQ (or dQᵀ) into TMEM buffer s & 1, once the drain of step s-2 freed it.
@@ -316,16 +326,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           if (!ok) break;
           tc::fence_after_sync();
         }
-        const uint32_t dq_col = C::kColDQ + st * C::kDqCols;
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t km = kk * 2048;   // 16 keys down both MN-major operands
-          if (C::kDqTransposed)   // dQᵀ = K_jᵀ dSᵀ: A = K_j (MN-major, d atoms), B = dSᵀ
-            tc::mma_ss(tmem + dq_col, tc::smem_desc(k_s + km, kBK * 128, 1024, tc::kLayoutSW128),
-                       tc::smem_desc(sa + km, kBK * 128, 1024, tc::kLayoutSW128), idesc_dq, kk > 0);
-          else                    // dQ = dS K_j: A = dSᵀ (MN-major, query atoms), B = K_j
-            tc::mma_ss(tmem + dq_col, tc::smem_desc(sa + km, kBK * 128, 1024, tc::kLayoutSW128),
-                       tc::smem_desc(k_s + km, kBK * 128, 1024, tc::kLayoutSW128), idesc_dq, kk > 0);
+        {
+          const uint32_t dq_col = C::kColDQ + st * C::kDqCols;
+          // dQᵀ = K_jᵀ dSᵀ (A = K_j MN-major over d atoms, B = dSᵀ) for d = 128;
+          // dQ = dS K_j (A = dSᵀ MN-major over query atoms, B = K_j) for d = 64.
+          const uint64_t k_mn = tc::smem_desc(k_s, kBK * 128, 1024, tc::kLayoutSW128);
+          const uint64_t s_mn = tc::smem_desc(sa, kBK * 128, 1024, tc::kLayoutSW128);
+          const uint64_t a0 = C::kDqTransposed ? k_mn : s_mn;
+          const uint64_t b0 = C::kDqTransposed ? s_mn : k_mn;
+#pragma unroll 1
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t step = uint64_t(kk * 2048) >> 4;   // 16 keys down both operands
+            tc::mma_ss(tmem + dq_col, a0 + step, b0 + step, idesc_dq, kk > 0);
+          }
         }
         tc::mma_commit(&bars.dq_full[st]);
         tc::mma_commit(&bars.ps_free[pb]);
@@ -338,8 +351,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tc::mma_commit(&bars.mma_drain);
       mbar_wait_bounded(&bars.mma_drain, 0, nullptr);
     }
+  } else if (warp == 3) {
+    regs_dec<88>();                                    // idle warp of the first warpgroup
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroup
+    regs_inc<216>();
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // key row in the tile (TMEM lane)
     const int key = k0 + r;
@@ -365,34 +381,48 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const bool key_in = key < Nk;
       // first visible query column of this key row (causal), relative to q0
       const int qmin = causal ? key - shift - q0 : -1;
+      const bool masked_row = !key_in || qmin > 0;
+      const f2 c2{c, c};
 #pragma unroll
-      for (int half = 0; half < BQ / 32; ++half) {
-        uint32_t sr[32], dr[32];
-        tc::tmem_ld32(tmem + lane_base + C::kColS + half * 32, sr);
-        tc::tmem_ld32(tmem + lane_base + C::kColDP + half * 32, dr);
+      for (int chunk = 0; chunk < BQ / 64; ++chunk) {
+        uint32_t s0[32], s1[32], d0[32], d1[32];
+        const uint32_t col0 = chunk * 64;
+        tc::tmem_ld32(tmem + lane_base + C::kColS + col0, s0);
+        tc::tmem_ld32(tmem + lane_base + C::kColS + col0 + 32, s1);
+        tc::tmem_ld32(tmem + lane_base + C::kColDP + col0, d0);
+        tc::tmem_ld32(tmem + lane_base + C::kColDP + col0 + 32, d1);
         tc::tmem_ld_wait();
-        uint32_t pk[16], dk[16];
+        auto sr = [&](int i) { return i < 32 ? s0[i] : s1[i - 32]; };
+        auto dr = [&](int i) { return i < 32 ? d0[i] : d1[i - 32]; };
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float pv[2], dv[2];
+        for (int g8 = 0; g8 < 8; ++g8) {          // 8 columns = one 16-byte chunk of Pᵀ / dSᵀ
+          uint32_t pk[4], dk[4];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = half * 32 + 2 * e + u;
-            const float l2 = vec[col];
-            float p = fast_exp2(fmaf(__uint_as_float(sr[2 * e + u]), c, -l2));
-            if (!key_in || col < qmin) p = 0.f;
-            pv[u] = p;
-            dv[u] = p * (__uint_as_float(dr[2 * e + u]) - vec[BQ + col]);
+          for (int h4 = 0; h4 < 2; ++h4) {
+            const int cb = g8 * 8 + h4 * 4;         // column within the chunk
+            const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + cb);       // -LSE·log2e
+            const float4 nd = *reinterpret_cast<const float4*>(vec + BQ + col0 + cb);  // -D
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int e = cb + 2 * u;
+              f2 x = fma2(f2{__uint_as_float(sr(e)), __uint_as_float(sr(e + 1))}, c2,
+                          u == 0 ? f2{nl.x, nl.y} : f2{nl.z, nl.w});
+              f2 p{fast_exp2(x.x), fast_exp2(x.y)};
+              if (masked_row) {
+                const int col = col0 + e;
+                if (!key_in || col < qmin) p.x = 0.f;
+                if (!key_in || col + 1 < qmin) p.y = 0.f;
+              }
+              const f2 dpd = add2(f2{__uint_as_float(dr(e)), __uint_as_float(dr(e + 1))},
+                                  u == 0 ? f2{nd.x, nd.y} : f2{nd.z, nd.w});
+              const f2 ds = mul2(p, dpd);
+              pk[h4 * 2 + u] = pack_bf16x2(p.x, p.y);
+              dk[h4 * 2 + u] = pack_bf16x2(ds.x, ds.y);
+            }
           }
-          pk[e] = pack_bf16x2(pv[0], pv[1]);
-          dk[e] = pack_bf16x2(dv[0], dv[1]);
-        }
-        // 32 columns = 4 chunks of 16 bytes in row r
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t off = sw128_offset(r, half * 32 + u * 8, kBK);
-          *reinterpret_cast<uint4*>(pt + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(dst + off) = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+          const uint32_t off = sw128_offset(r, col0 + g8 * 8, kBK);
+          *reinterpret_cast<uint4*>(pt + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(dst + off) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
         }
       }
       fence_proxy_async_smem();      // generic-proxy writes -> tensor-core (async proxy) reads
@@ -405,6 +435,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (warp >= 8) {
     // ---------------------------------------------------------- dQ drain, dK/dV epilogue
+    regs_inc<200>();
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;

@@ -48,7 +48,7 @@ constexpr size_t decode_smem_bytes() {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
@@ -94,8 +94,10 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   if (tid == 0)
     for (; issued < min(kStages, nstages); ++issued) issue(issued);
 
-  // Query slice of this lane for all G heads, pre-scaled into log2 units.
-  float qf[G][NV * 8];
+  // Query slice of this lane for all G heads, pre-scaled into log2 units,
+  // as pairs of consecutive dimensions (packed f32x2 arithmetic).
+  constexpr int NP = NV * 4;                       // dimension pairs per lane
+  f2 qf[G][NP];
   const float qs = scale * kLog2e;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -105,21 +107,20 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
       const uint4 w = *reinterpret_cast<const uint4*>(qh + 64 * vv + 8 * sub);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        qf[h][vv * 8 + 2 * e] = bf16lo(ws[e]) * qs;
-        qf[h][vv * 8 + 2 * e + 1] = bf16hi(ws[e]) * qs;
-      }
+      for (int e = 0; e < 4; ++e) qf[h][vv * 4 + e] = f2{bf16lo(ws[e]) * qs, bf16hi(ws[e]) * qs};
     }
   }
 
-  float acc[G][NV * 8];
-  float m_run[G], l_run[G];
+  // Per group: reference max (log2 units; moved lazily), denominator, and
+  // un-normalised output, all relative to the reference.
+  f2 acc[G][NP];
+  float m_ref[G], l_run[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    m_run[h] = -INFINITY;
+    m_ref[h] = -INFINITY;
     l_run[h] = 0.f;
 #pragma unroll
-    for (int e = 0; e < NV * 8; ++e) acc[h][e] = 0.f;
+    for (int e = 0; e < NP; ++e) acc[h][e] = f2{0.f, 0.f};
   }
 
   bool ok = true;
@@ -146,64 +147,82 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 
     // This group's two keys of the stage: warp*8 + grp and warp*8 + grp + 4.
     float sc[2][G];
-    uint4 vrow[2][NV];
+    int krow[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int kk = warp * 8 + grp + 4 * r;
       const bool valid = kk < rows;
       const int kr = valid ? kk : 0;
-      float part[G];
+      krow[r] = kr;
+      f2 part[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h) part[h] = 0.f;
+      for (int h = 0; h < G; ++h) part[h] = f2{0.f, 0.f};
 #pragma unroll
       for (int vv = 0; vv < NV; ++vv) {
         const uint4 w = *reinterpret_cast<const uint4*>(kb + kr * kRowBytes + (64 * vv + 8 * sub) * 2);
-        vrow[r][vv] = *reinterpret_cast<const uint4*>(vb + kr * kRowBytes + (64 * vv + 8 * sub) * 2);
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float k0 = bf16lo(ws[e]), k1 = bf16hi(ws[e]);
+          const f2 kv{bf16lo(ws[e]), bf16hi(ws[e])};
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            part[h] = fmaf(qf[h][vv * 8 + 2 * e], k0, part[h]);
-            part[h] = fmaf(qf[h][vv * 8 + 2 * e + 1], k1, part[h]);
-          }
+          for (int h = 0; h < G; ++h) part[h] = fma2(qf[h][vv * 4 + e], kv, part[h]);
         }
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float x = part[h];
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        sc[r][h] = valid ? x : -INFINITY;
+        float xsum = part[h].x + part[h].y;
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 4);
+        sc[r][h] = valid ? xsum : -INFINITY;
       }
     }
 
-    // Online update of (m, l, o) for this group's two keys.
+    // Online update of (m, l, o) for this group's two keys. The reference max
+    // moves only when a score exceeds it by more than 2^8 (exact either way,
+    // since l and o share the reference).
+    bool need[G];
+    bool any_need = false;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float m_new = fmaxf(m_run[h], fmaxf(sc[0][h], sc[1][h]));
-      if (m_new == -INFINITY) continue;  // nothing visible yet in this group
-      const float alpha = fast_exp2(m_run[h] - m_new);   // 0 when m_run = -inf
-      const float p0 = fast_exp2(sc[0][h] - m_new);
-      const float p1 = fast_exp2(sc[1][h] - m_new);
-      l_run[h] = fmaf(alpha, l_run[h], p0 + p1);
-      m_run[h] = m_new;
+      need[h] = max3(m_ref[h], sc[0][h], sc[1][h]) > m_ref[h] + 8.f;   // true from -inf too
+      any_need |= need[h];
+    }
+    if (__any_sync(0xffffffffu, any_need)) {
 #pragma unroll
-      for (int vv = 0; vv < NV; ++vv) {
-        const uint32_t w0[4] = {vrow[0][vv].x, vrow[0][vv].y, vrow[0][vv].z, vrow[0][vv].w};
-        const uint32_t w1[4] = {vrow[1][vv].x, vrow[1][vv].y, vrow[1][vv].z, vrow[1][vv].w};
+      for (int h = 0; h < G; ++h) {
+        const float m_new = need[h] ? max3(m_ref[h], sc[0][h], sc[1][h]) : m_ref[h];
+        const float alpha = need[h] ? fast_exp2(m_ref[h] - m_new) : 1.f;   // 0 from -inf
+        m_ref[h] = m_new;
+        l_run[h] *= alpha;
+        const f2 a2{alpha, alpha};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float& a0 = acc[h][vv * 8 + 2 * e];
-          float& a1 = acc[h][vv * 8 + 2 * e + 1];
-          a0 = fmaf(p1, bf16lo(w1[e]), fmaf(p0, bf16lo(w0[e]), a0 * alpha));
-          a1 = fmaf(p1, bf16hi(w1[e]), fmaf(p0, bf16hi(w0[e]), a1 * alpha));
-        }
+        for (int e = 0; e < NP; ++e) acc[h][e] = mul2(acc[h][e], a2);
       }
     }
-
+    f2 p2[2][G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float nm = (m_ref[h] == -INFINITY) ? 0.f : -m_ref[h];
+      const float p0 = fast_exp2(sc[0][h] + nm);
+      const float p1 = fast_exp2(sc[1][h] + nm);
+      l_run[h] += p0 + p1;
+      p2[0][h] = f2{p0, p0};
+      p2[1][h] = f2{p1, p1};
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv) {
+        const uint4 x = *reinterpret_cast<const uint4*>(vb + krow[r] * kRowBytes + (64 * vv + 8 * sub) * 2);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const f2 v2{bf16lo(xs[e]), bf16hi(xs[e])};
+#pragma unroll
+          for (int h = 0; h < G; ++h) acc[h][vv * 4 + e] = fma2(v2, p2[r][h], acc[h][vv * 4 + e]);
+        }
+      }
   }
   if (!ok) return;
 
@@ -216,7 +235,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   if (sub == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      sm_m[gid * G + h] = m_run[h];
+      sm_m[gid * G + h] = m_ref[h];
       sm_l[gid * G + h] = l_run[h];
     }
   }
@@ -225,7 +244,11 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 #pragma unroll
     for (int vv = 0; vv < NV; ++vv)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sm_o[(gid * G + h) * D + 64 * vv + 8 * sub + e] = acc[h][vv * 8 + e];
+      for (int e = 0; e < 4; ++e) {
+        float* dst = sm_o + (gid * G + h) * D + 64 * vv + 8 * sub + 2 * e;
+        dst[0] = acc[h][vv * 4 + e].x;
+        dst[1] = acc[h][vv * 4 + e].y;
+      }
   __syncthreads();
 
   for (int idx = tid; idx < G * D; idx += kThreads) {

@@ -318,10 +318,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         for (int cc = 0; cc < kBN; ++cc)
           if (key0 + cc > limit) s[cc] = -INFINITY;
       }
-      float mx = max3(s[0], s[1], s[2]);
+      // Row max as 8 independent chains (short dependency chains, more ILP).
+      float m8[8];
 #pragma unroll
-      for (int cc = 3; cc < kBN - 1; cc += 2) mx = max3(mx, s[cc], s[cc + 1]);
-      mx = fmaxf(mx, s[kBN - 1]);
+      for (int k = 0; k < 8; ++k) m8[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+      for (int i = 16; i < kBN; i += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[i + k], s[i + 8 + k]);
+      const float mx = fmaxf(max3(m8[0], m8[1], m8[2]),
+                             fmaxf(max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_cand = fmaxf(m_ref, mx * c);
       const bool need = m_cand - m_ref > kRescaleThreshold;   // also true while m_ref = -inf
       float alpha = 1.f;
@@ -333,7 +339,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
       // P̃ = exp2(s·c - m_ref) -> bf16 pairs into the first 64 columns of S.
       const f2 cc2{c, c}, nm2{neg_m, neg_m};
-      f2 rs2{0.f, 0.f};
+      f2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // 4 independent sums
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
@@ -342,12 +348,13 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           f2 x = fma2(f2{s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]}, cc2, nm2);
           x.x = fast_exp2(x.x);
           x.y = fast_exp2(x.y);
-          rs2 = add2(rs2, x);
+          rs2[e & 3] = add2(rs2[e & 3], x);
           pk[e] = pack_bf16x2(x.x, x.y);
         }
         tmem_st32(s_addr + half * 32, pk);
       }
-      const float rs = rs2.x + rs2.y;
+      const f2 rsa = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
+      const float rs = rsa.x + rsa.y;
       l_run = fmaf(alpha, l_run, rs);
 
       // Rescale Õ (once the previous P̃V has landed) when the reference moved.
