@@ -44,41 +44,54 @@ ATTN_DEFINE_ERROR_WORD(take_error_bwd_tc)
 namespace {
 
 constexpr int kBK = 128;            // keys per CTA (TMEM lanes)
-constexpr int kThreads = 384;       // 12 warps
+constexpr int kThreads = 512;       // 16 warps
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
   static constexpr int BQ = (D == 128) ? 64 : 128;        // query rows per step
   static constexpr bool kDqTransposed = (D == 128);       // dQᵀ (M = d) vs dQ (M = BQ)
-  static constexpr int kPsBufs = (D == 128) ? 2 : 1;      // Pᵀ/dSᵀ shared-memory buffers
-  static constexpr int kQStages = 2;
+  static constexpr int kPsBufs = (D == 128) ? 2 : 1;      // dSᵀ shared-memory buffers
+  static constexpr int kQStages = 3;                       // Q_i, dO_i, LSE, D ring
   // shared memory (bytes; every tile 1024-aligned)
   static constexpr int kKVTile = kBK * D * 2;             // K_j or V_j
   static constexpr int kQTile = BQ * D * 2;               // Q_i or dO_i
-  static constexpr int kPsTile = kBK * BQ * 2;            // Pᵀ or dSᵀ
+  static constexpr int kPsTile = kBK * BQ * 2;            // dSᵀ (bf16, the B operand of dQ)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVTile;
   static constexpr int kOffQ = kOffV + kKVTile;                      // [stage] Q, dO
-  static constexpr int kOffP = kOffQ + kQStages * 2 * kQTile;       // [buf] Pᵀ, dSᵀ
-  static constexpr int kOffVec = kOffP + kPsBufs * 2 * kPsTile;     // [stage] LSE2, D
+  static constexpr int kOffP = kOffQ + kQStages * 2 * kQTile;       // [buf] dSᵀ
+  static constexpr int kOffVec = kOffP + kPsBufs * kPsTile;         // [stage] -LSE·log2e, -D
   static constexpr int kSmemBytes = kOffVec + kQStages * 2 * BQ * 4;
   static constexpr int kDynSmem = kSmemBytes + 1024;
-  // tensor memory columns
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = BQ;
-  static constexpr uint32_t kColDQ = 2 * BQ;                         // 2 buffers
+  // tensor memory columns. d = 128: two (Sᵀ, dPᵀ) buffers of 64 + 64
+  // columns; dQᵀ(s) is written over the Sᵀ columns of its own buffer once the
+  // softmax has read them; dV, dK 128 each (2·128 + 2·128 = 512). d = 64:
+  // one (Sᵀ, dPᵀ) buffer of 128 + 128, two dQ buffers of 64, dV, dK 64 each.
+  static constexpr int kSdpBufs = (D == 128) ? 2 : 1;
+  static constexpr bool kDqInS = (D == 128);
+  static constexpr uint32_t kSdpCols = 2 * BQ;
+  static constexpr uint32_t kColDQ = kSdpBufs * kSdpCols;            // d = 64 only
   static constexpr uint32_t kDqCols = kDqTransposed ? BQ : D;
-  static constexpr uint32_t kColDV = kColDQ + 2 * kDqCols;
+  static constexpr uint32_t kColDV = kDqInS ? kSdpBufs * kSdpCols : kColDQ + 2 * kDqCols;
   static constexpr uint32_t kColDK = kColDV + D;
   static_assert(kColDK + D <= 512, "TMEM budget");
+  __host__ __device__ static constexpr uint32_t col_s(int b) { return b * kSdpCols; }
+  __host__ __device__ static constexpr uint32_t col_dp(int b) { return b * kSdpCols + BQ; }
+  // Pᵀ and dSᵀ (bf16 pairs) are written over the consumed Sᵀ / dPᵀ columns:
+  // the warpgroup owning query columns [CW·h, CW·h + CW) stores its pairs at
+  // columns [CW·h, CW·h + CW/2) of the buffer. Column of query q0 (multiple of 16):
+  static constexpr int CW = BQ / 2;
+  __host__ __device__ static constexpr uint32_t col_pair(int q0) {
+    return (q0 / CW) * CW + (q0 % CW) / 2;
+  }
   static_assert(kDynSmem <= 232448, "shared-memory budget");
 };
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t sdp_full, p_full;
+  uint64_t q_full[3], q_empty[3];
+  uint64_t sdp_full[2], p_full[2];
   uint64_t ps_free[2];
   uint64_t dq_full[2], dq_free[2];
   uint64_t dkv_full, mma_drain;
@@ -162,15 +175,22 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   if (tid == 0) {
     bars.abort = 0;
     mbar_init(&bars.kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kQStages; ++i) {
       mbar_init(&bars.q_full[i], 1 + 32);   // TMA producer + 32 LSE/D loader lanes
       mbar_init(&bars.q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.ps_free[i], 1);
       mbar_init(&bars.dq_full[i], 1);
       mbar_init(&bars.dq_free[i], 128);
     }
-    mbar_init(&bars.sdp_full, 1);
-    mbar_init(&bars.p_full, 128);
+    mbar_init(&bars.sdp_full[0], 1);
+    mbar_init(&bars.sdp_full[1], 1);
+    // two p_full barriers (step parity): the softmax of step s+1 may finish
+    // before the MMA thread has observed step s, which a single barrier would
+    // alias; step s+2 cannot (its Sᵀ/dPᵀ are issued after step s is consumed)
+    mbar_init(&bars.p_full[0], 256);     // both Pᵀ/dSᵀ warpgroups
+    mbar_init(&bars.p_full[1], 256);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.mma_drain, 1);
     fence_barrier_init();
@@ -185,12 +205,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
-  // Register split, set inside each role (launch: 384 x 168): warps 0-3
-  // (TMA, MMA, LSE/D loader, idle) 88; Pᵀ/dSᵀ warpgroup 216; dQ/epilogue
-  // warpgroup 200. 128 x (88 + 216 + 200) = 384 x 168.
+  // Register split, set inside each role (launch: 512 x 128): warps 0-3
+  // (TMA, MMA, LSE/D loader, idle) 120; the two Pᵀ/dSᵀ warpgroups 136 each;
+  // the dQ/epilogue warpgroup 120. 128 x (120 + 136 + 136 + 120) = 512 x 128.
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
-    regs_dec<88>();
+    regs_dec<120>();
     if (lane == 0 && n > 0) {
       tc::tma_prefetch_desc(&map_q);
       tc::tma_prefetch_desc(&map_do);
@@ -202,8 +222,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       int issued = 0;
       bool ok = true;
       for (int s = 0; s < n && ok; ++s) {
-        const int st = s & 1;
-        if (s >= 2) ok = mbar_wait_bounded(&bars.q_empty[st], ((s >> 1) - 1) & 1, abort_flag);
+        const int st = s % C::kQStages;
+        if (s >= C::kQStages)
+          ok = mbar_wait_bounded(&bars.q_empty[st], ((s / C::kQStages) - 1) & 1, abort_flag);
         if (!ok) break;
         int hh, qt;
         plan.at(s, hh, qt);
@@ -221,33 +242,47 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         attn_flag_error(kErrTimeout);
         bars.abort = 1;
         mbar_wait_bounded(&bars.kv_full, 0, nullptr);
-        for (int s = max(0, issued - 2); s < issued; ++s)
-          mbar_wait_bounded(&bars.q_full[s & 1], (s >> 1) & 1, nullptr);
+        for (int s = max(0, issued - C::kQStages); s < issued; ++s)
+          mbar_wait_bounded(&bars.q_full[s % C::kQStages], (s / C::kQStages) & 1, nullptr);
       }
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------- LSE / D loader
-    regs_dec<88>();
+    regs_dec<120>();
     // Per step: -LSE·log2e and -D of the BQ query rows into the stage's
     // vectors; rows past Nq get -LSE·log2e = -inf (P = 0) and -D = 0.
-    bool ok = true;
-    for (int s = 0; s < n && ok; ++s) {
-      const int st = s & 1;
-      if (s >= 2)
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded(&bars.q_empty[st], ((s >> 1) - 1) & 1, abort_flag));
-      if (!ok) break;
+    // The global loads of a step are issued before waiting for its stage to
+    // free up, so their latency overlaps the wait.
+    constexpr int kPer = BQ / 32;
+    float nl[kPer], nd[kPer];
+    auto fetch = [&](int s) {
       int hh, qt;
       plan.at(s, hh, qt);
       const size_t bh = size_t(b) * Hq + g * group + hh;
-      float* vec = reinterpret_cast<float*>(smem + C::kOffVec + st * 2 * BQ * 4);
-      for (int c = lane; c < BQ; c += 32) {
-        const int q = qt * BQ + c;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int q = qt * BQ + u * 32 + lane;
         const bool in = q < Nq;
-        vec[c] = in ? -lse[bh * Nq + q] * kLog2e : -INFINITY;
-        vec[BQ + c] = in ? -row_term[bh * Nq + q] : 0.f;
+        nl[u] = in ? -lse[bh * Nq + q] * kLog2e : -INFINITY;
+        nd[u] = in ? -row_term[bh * Nq + q] : 0.f;
+      }
+    };
+    bool ok = true;
+    if (n > 0) fetch(0);
+    for (int s = 0; s < n && ok; ++s) {
+      const int st = s % C::kQStages;
+      if (s >= C::kQStages)
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.q_empty[st],
+                                                       ((s / C::kQStages) - 1) & 1, abort_flag));
+      if (!ok) break;
+      float* vec = reinterpret_cast<float*>(smem + C::kOffVec + st * 2 * BQ * 4);
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        vec[u * 32 + lane] = nl[u];
+        vec[BQ + u * 32 + lane] = nd[u];
       }
       mbar_arrive(&bars.q_full[st]);
+      if (s + 1 < n) fetch(s + 1);
     }
     if (!ok && lane == 0) {
       attn_flag_error(kErrTimeout);
@@ -255,93 +290,145 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    regs_dec<88>();
+    regs_dec<120>();
     if (lane == 0) {
       constexpr uint32_t idesc_sdp = tc::idesc_bf16_f32(kBK, BQ, false, false);
       constexpr uint32_t idesc_kv = tc::idesc_bf16_f32(kBK, D, false, true);
       constexpr uint32_t idesc_dq = C::kDqTransposed ? tc::idesc_bf16_f32(D, BQ, true, true)
                                                      : tc::idesc_bf16_f32(BQ, D, true, true);
-      const uint32_t k_s = smem_u32(smem + C::kOffK);
-      const uint32_t v_s = smem_u32(smem + C::kOffV);
-      bool ok = true;
-
+      // Base descriptors; a descriptor's start-address field is (bytes >> 4),
+      // so moving inside a tile adds (offset >> 4) to the 64-bit value.
+      const uint64_t k_km = tc::smem_desc(smem_u32(smem + C::kOffK), 16, 1024, tc::kLayoutSW128);
+      const uint64_t v_km = tc::smem_desc(smem_u32(smem + C::kOffV), 16, 1024, tc::kLayoutSW128);
+      const uint64_t k_mn = tc::smem_desc(smem_u32(smem + C::kOffK), kBK * 128, 1024, tc::kLayoutSW128);
+      auto q_km = [&](int st, int which) {   // Q (0) or dO (1) of a stage, K-major
+        return tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2 + which) * C::kQTile), 16, 1024,
+                             tc::kLayoutSW128);
+      };
+      auto q_mn = [&](int st, int which) {   // the same tile as an MN-major operand
+        return tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2 + which) * C::kQTile), BQ * 128,
+                             1024, tc::kLayoutSW128);
+      };
+      auto ps_mn = [&](int pb) {              // dSᵀ as an MN-major operand
+        return tc::smem_desc(smem_u32(smem + C::kOffP + pb * C::kPsTile), kBK * 128, 1024,
+                             tc::kLayoutSW128);
+      };
       auto issue_sdp = [&](int s) {   // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ (all operands K-major)
-        const uint32_t qa = smem_u32(smem + C::kOffQ + (s & 1) * 2 * C::kQTile);
-        const uint32_t da = qa + C::kQTile;
-#pragma unroll 1
+        const int st = s % C::kQStages;
+        const int b = s % C::kSdpBufs;
+        const uint64_t qd = q_km(st, 0), dd = q_km(st, 1);
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // K_j / V_j
-          const uint32_t qb = (kk / 4) * (BQ * 128) + (kk % 4) * 32;    // Q_i / dO_i
-          tc::mma_ss(tmem + C::kColS, tc::smem_desc(k_s + ka, 16, 1024, tc::kLayoutSW128),
-                     tc::smem_desc(qa + qb, 16, 1024, tc::kLayoutSW128), idesc_sdp, kk > 0);
-          tc::mma_ss(tmem + C::kColDP, tc::smem_desc(v_s + ka, 16, 1024, tc::kLayoutSW128),
-                     tc::smem_desc(da + qb, 16, 1024, tc::kLayoutSW128), idesc_sdp, kk > 0);
+          const uint64_t ka = ((kk / 4) * (kBK * 128) + (kk % 4) * 32) >> 4;   // K_j / V_j
+          const uint64_t qb = ((kk / 4) * (BQ * 128) + (kk % 4) * 32) >> 4;    // Q_i / dO_i
+          tc::mma_ss(tmem + C::col_s(b), k_km + ka, qd + qb, idesc_sdp, kk > 0);
+          tc::mma_ss(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
         }
-        tc::mma_commit(&bars.sdp_full);
+        tc::mma_commit(&bars.sdp_full[b]);
       };
 
-      if (n > 0) {
-        ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
-        if (ok) ok = mbar_wait_bounded(&bars.q_full[0], 0, abort_flag);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_sdp(0);
-        }
-      }
-      for (int s = 0; s < n && ok; ++s) {
-        const int st = s & 1;
-        const int pb = s % C::kPsBufs;
-        ok = mbar_wait_bounded(&bars.p_full, s & 1, abort_flag);
+      bool ok = true;
+      if (n > 0) ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
+      for (int j = 0; j < C::kSdpBufs && j < n && ok; ++j) {
+        ok = mbar_wait_bounded(&bars.q_full[j % C::kQStages], (j / C::kQStages) & 1, abort_flag);
         if (!ok) break;
         tc::fence_after_sync();
-        if (s + 1 < n) {
-          ok = mbar_wait_bounded(&bars.q_full[(s + 1) & 1], ((s + 1) >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_sdp(s + 1);
-        }
-        const uint32_t qa = smem_u32(smem + C::kOffQ + st * 2 * C::kQTile);
-        const uint32_t da = qa + C::kQTile;
-        const uint32_t pa = smem_u32(smem + C::kOffP + pb * 2 * C::kPsTile);
-        const uint32_t sa = pa + C::kPsTile;
-        // dV += Pᵀ dO ; dK += dSᵀ Q   (M = keys, N = d, K = BQ queries)
+        issue_sdp(j);
+      }
+      // dV += Pᵀ dO ; dK += dSᵀ Q ; dQ(ᵀ)   for step s (after its p_full)
+      auto issue_grads = [&](int s) {
+        const int st = s % C::kQStages;
+        const int pb = s % C::kPsBufs;
+        const int b = s % C::kSdpBufs;
+        const int db = s & 1;
         {
-          const uint64_t dv_b = tc::smem_desc(da, BQ * 128, 1024, tc::kLayoutSW128);  // dO MN-major
-          const uint64_t dk_b = tc::smem_desc(qa, BQ * 128, 1024, tc::kLayoutSW128);  // Q MN-major
-#pragma unroll 1
+          // A = Pᵀ / dSᵀ from tensor memory (bf16 pairs), B = dO / Q MN-major
+          const uint64_t dob = q_mn(st, 1), qb = q_mn(st, 0);
+#pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
-            const uint32_t pk = (kk / 4) * (kBK * 128) + (kk % 4) * 32;   // Pᵀ/dSᵀ K-major
-            const uint64_t step = uint64_t(kk * 2048) >> 4;               // 16 query rows down
+            const uint32_t ac = C::col_pair(kk * 16);
+            const uint64_t step = uint64_t(kk * 2048) >> 4;                      // 16 query rows
             const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-            tc::mma_ss(tmem + C::kColDV, tc::smem_desc(pa + pk, 16, 1024, tc::kLayoutSW128),
-                       dv_b + step, idesc_kv, acc);
-            tc::mma_ss(tmem + C::kColDK, tc::smem_desc(sa + pk, 16, 1024, tc::kLayoutSW128),
-                       dk_b + step, idesc_kv, acc);
+            tc::mma_ts(tmem + C::kColDV, tmem + C::col_s(b) + ac, dob + step, idesc_kv, acc);
+            tc::mma_ts(tmem + C::kColDK, tmem + C::col_dp(b) + ac, qb + step, idesc_kv, acc);
           }
         }
-        tc::mma_commit(&bars.q_empty[st]);
-        // dQ (or dQᵀ) into TMEM buffer s & 1, once the drain of step s-2 freed it.
-        if (s >= 2) {
-          ok = mbar_wait_bounded(&bars.dq_free[st], ((s >> 1) - 1) & 1, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-        }
+        tc::mma_commit(&bars.q_empty[st]);           // Q_i, dO_i, LSE, D of the stage consumed
         {
-          const uint32_t dq_col = C::kColDQ + st * C::kDqCols;
           // dQᵀ = K_jᵀ dSᵀ (A = K_j MN-major over d atoms, B = dSᵀ) for d = 128;
           // dQ = dS K_j (A = dSᵀ MN-major over query atoms, B = K_j) for d = 64.
-          const uint64_t k_mn = tc::smem_desc(k_s, kBK * 128, 1024, tc::kLayoutSW128);
-          const uint64_t s_mn = tc::smem_desc(sa, kBK * 128, 1024, tc::kLayoutSW128);
+          const uint32_t dq_col = C::kDqInS ? C::col_s(b) : C::kColDQ + db * C::kDqCols;
+          const uint64_t s_mn = ps_mn(pb);
           const uint64_t a0 = C::kDqTransposed ? k_mn : s_mn;
           const uint64_t b0 = C::kDqTransposed ? s_mn : k_mn;
-#pragma unroll 1
+#pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t step = uint64_t(kk * 2048) >> 4;   // 16 keys down both operands
             tc::mma_ss(tmem + dq_col, a0 + step, b0 + step, idesc_dq, kk > 0);
           }
         }
-        tc::mma_commit(&bars.dq_full[st]);
+        tc::mma_commit(&bars.dq_full[db]);
         tc::mma_commit(&bars.ps_free[pb]);
+      };
+
+      if (C::kSdpBufs == 1) {
+        // One (Sᵀ, dPᵀ) buffer, which also holds Pᵀ, dSᵀ of the step: the
+        // gradients of step s are issued first, then the buffer is refilled
+        // with step s+1 (the tensor pipe executes in issue order).
+        for (int s = 0; s < n && ok; ++s) {
+          ok = mbar_wait_bounded(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+          if (s >= 2) {   // dQ TMEM buffer s & 1 drained (step s-2)
+            ok = mbar_wait_bounded(&bars.dq_free[s & 1], ((s >> 1) - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+          }
+          issue_grads(s);
+          if (s + 1 < n) {
+            const int s1 = s + 1;
+            ok = mbar_wait_bounded(&bars.q_full[s1 % C::kQStages], (s1 / C::kQStages) & 1,
+                                   abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_sdp(s1);
+          }
+        }
+      } else {
+        // Two buffers: a greedy issuer. tcgen05.mma issue stalls once the
+        // tensor pipe's queue is full, so the thread must never sit on one
+        // barrier while other work is ready. Work items: Sᵀ/dPᵀ of step t
+        // (buffer t & 1 drained of dQᵀ(t-2), Q/dO(t) loaded) and the
+        // gradients of step s (its softmax done). Sᵀ/dPᵀ first: it feeds the
+        // softmax warpgroups.
+        int s = 0, t = min(C::kSdpBufs, n);
+        uint64_t t_last = global_timer_ns();   // bounded: no progress for the wait limit = abort
+        uint32_t spins = 0;
+        while (s < n) {
+          if (t < n && t - 2 < s &&
+              mbar_try_wait(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1) &&
+              mbar_try_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1)) {
+            tc::fence_after_sync();
+            issue_sdp(t);
+            ++t;
+            spins = 0;
+            t_last = global_timer_ns();
+            continue;
+          }
+          if (mbar_try_wait(&bars.p_full[s & 1], (s >> 1) & 1)) {
+            tc::fence_after_sync();
+            issue_grads(s);
+            ++s;
+            spins = 0;
+            t_last = global_timer_ns();
+            continue;
+          }
+          if ((++spins & 255u) == 0 &&
+              (*abort_flag || global_timer_ns() - t_last > kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) {
         attn_flag_error(kErrTimeout);
@@ -352,60 +439,61 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       mbar_wait_bounded(&bars.mma_drain, 0, nullptr);
     }
   } else if (warp == 3) {
-    regs_dec<88>();                                    // idle warp of the first warpgroup
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroup
-    regs_inc<216>();
+    regs_dec<120>();                                    // idle warp of the first warpgroup
+  } else if (warp >= 4 && warp < 12) {
+    // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroups
+    // Two warpgroups share the key rows (TMEM lanes) and split the BQ query
+    // columns of each step in halves.
+    regs_inc<136>();
+    constexpr int CW = BQ / 2;                         // columns per warpgroup
+    const int half = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // key row in the tile (TMEM lane)
     const int key = k0 + r;
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const float c = scale * kLog2e;
     const int shift = Nk - Nq;
+    const int cbase = half * CW;
     bool ok = true;
     for (int s = 0; s < n; ++s) {
-      const int st = s & 1;
+      const int st = s % C::kQStages;
       const int pb = s % C::kPsBufs;
       int hh, qt;
       plan.at(s, hh, qt);
       const int q0 = qt * BQ;
-      bool w = mbar_wait_bounded(&bars.sdp_full, s & 1, abort_flag);
-      w = w && mbar_wait_bounded(&bars.q_full[st], (s >> 1) & 1, abort_flag);
+      const int b = s % C::kSdpBufs;
+      bool w = mbar_wait_bounded(&bars.sdp_full[b], (s / C::kSdpBufs) & 1, abort_flag);
+      w = w && mbar_wait_bounded(&bars.q_full[st], (s / C::kQStages) & 1, abort_flag);
       if (s >= C::kPsBufs)
         w = w && mbar_wait_bounded(&bars.ps_free[pb], ((s / C::kPsBufs) - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc::fence_after_sync();
       const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * BQ * 4);
-      uint8_t* pt = smem + C::kOffP + pb * 2 * C::kPsTile;
-      uint8_t* dst = pt + C::kPsTile;
+      uint8_t* dst = smem + C::kOffP + pb * C::kPsTile;
       const bool key_in = key < Nk;
       // first visible query column of this key row (causal), relative to q0
       const int qmin = causal ? key - shift - q0 : -1;
-      const bool masked_row = !key_in || qmin > 0;
+      const bool masked_row = !key_in || qmin > cbase;
       const f2 c2{c, c};
 #pragma unroll
-      for (int chunk = 0; chunk < BQ / 64; ++chunk) {
-        uint32_t s0[32], s1[32], d0[32], d1[32];
-        const uint32_t col0 = chunk * 64;
-        tc::tmem_ld32(tmem + lane_base + C::kColS + col0, s0);
-        tc::tmem_ld32(tmem + lane_base + C::kColS + col0 + 32, s1);
-        tc::tmem_ld32(tmem + lane_base + C::kColDP + col0, d0);
-        tc::tmem_ld32(tmem + lane_base + C::kColDP + col0 + 32, d1);
+      for (int chunk = 0; chunk < CW / 32; ++chunk) {
+        uint32_t sr[32], dr[32];
+        const int col0 = cbase + chunk * 32;
+        tc::tmem_ld32(tmem + lane_base + C::col_s(b) + col0, sr);
+        tc::tmem_ld32(tmem + lane_base + C::col_dp(b) + col0, dr);
         tc::tmem_ld_wait();
-        auto sr = [&](int i) { return i < 32 ? s0[i] : s1[i - 32]; };
-        auto dr = [&](int i) { return i < 32 ? d0[i] : d1[i - 32]; };
+        uint32_t pk[16], dk[16];                  // bf16 pairs of the 32 columns
 #pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {          // 8 columns = one 16-byte chunk of Pᵀ / dSᵀ
-          uint32_t pk[4], dk[4];
+        for (int g8 = 0; g8 < 4; ++g8) {          // 8 columns = one 16-byte chunk of dSᵀ
 #pragma unroll
           for (int h4 = 0; h4 < 2; ++h4) {
-            const int cb = g8 * 8 + h4 * 4;         // column within the chunk
+            const int cb = g8 * 8 + h4 * 4;         // column within the 32
             const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + cb);       // -LSE·log2e
             const float4 nd = *reinterpret_cast<const float4*>(vec + BQ + col0 + cb);  // -D
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int e = cb + 2 * u;
-              f2 x = fma2(f2{__uint_as_float(sr(e)), __uint_as_float(sr(e + 1))}, c2,
+              f2 x = fma2(f2{__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])}, c2,
                           u == 0 ? f2{nl.x, nl.y} : f2{nl.z, nl.w});
               f2 p{fast_exp2(x.x), fast_exp2(x.y)};
               if (masked_row) {
@@ -413,59 +501,89 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                 if (!key_in || col < qmin) p.x = 0.f;
                 if (!key_in || col + 1 < qmin) p.y = 0.f;
               }
-              const f2 dpd = add2(f2{__uint_as_float(dr(e)), __uint_as_float(dr(e + 1))},
+              const f2 dpd = add2(f2{__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])},
                                   u == 0 ? f2{nd.x, nd.y} : f2{nd.z, nd.w});
               const f2 ds = mul2(p, dpd);
-              pk[h4 * 2 + u] = pack_bf16x2(p.x, p.y);
-              dk[h4 * 2 + u] = pack_bf16x2(ds.x, ds.y);
+              pk[e >> 1] = pack_bf16x2(p.x, p.y);
+              dk[e >> 1] = pack_bf16x2(ds.x, ds.y);
             }
           }
           const uint32_t off = sw128_offset(r, col0 + g8 * 8, kBK);
-          *reinterpret_cast<uint4*>(pt + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(dst + off) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+          *reinterpret_cast<uint4*>(dst + off) =
+              make_uint4(dk[4 * g8], dk[4 * g8 + 1], dk[4 * g8 + 2], dk[4 * g8 + 3]);
         }
+        // Pᵀ and dSᵀ pairs over the columns just read (A operands of dV, dK)
+        tc::tmem_st16(tmem + lane_base + C::col_s(b) + C::col_pair(col0), pk);
+        tc::tmem_st16(tmem + lane_base + C::col_dp(b) + C::col_pair(col0), dk);
       }
+      tc::tmem_st_wait();
       fence_proxy_async_smem();      // generic-proxy writes -> tensor-core (async proxy) reads
       tc::fence_before_sync();
-      mbar_arrive(&bars.p_full);
+      mbar_arrive(&bars.p_full[s & 1]);
     }
     if (!ok) {
       if (lane == 0) attn_flag_error(kErrTimeout);
       bars.abort = 1;
     }
-  } else if (warp >= 8) {
+  } else {
     // ---------------------------------------------------------- dQ drain, dK/dV epilogue
-    regs_inc<200>();
+    regs_dec<120>();
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     bool ok = true;
     for (int s = 0; s < n; ++s) {
-      const int st = s & 1;
+      const int db = s & 1;
       int hh, qt;
       plan.at(s, hh, qt);
       const size_t bh = size_t(b) * Hq + g * group + hh;
       const int q0 = qt * BQ;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars.dq_full[st], (s >> 1) & 1, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars.dq_full[db], (s >> 1) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const uint32_t col0 = C::kColDQ + st * C::kDqCols;
+      const uint32_t col0 = C::kDqInS ? C::col_s(s % C::kSdpBufs) : C::kColDQ + db * C::kDqCols;
       uint32_t v0[32], v1[32];
       tc::tmem_ld32(tmem + lane_base + col0, v0);
       tc::tmem_ld32(tmem + lane_base + col0 + 32, v1);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
-      mbar_arrive(&bars.dq_free[st]);
+      mbar_arrive(&bars.dq_free[db]);
       if (C::kDqTransposed) {
-        // lane r = dimension, columns = the BQ (= 64) query rows of the step
-        float* base = dq_acc + (bh * Nq + q0) * D + r;
+        // lane r = dimension, columns = the BQ (= 64) query rows of the step.
+        // A 4x4 transpose inside each quad of lanes gives every lane four
+        // consecutive dimensions of one query row, added into the float32
+        // accumulator with one 16-byte reduction: 16 per lane per step.
+        const int i4 = lane & 3;
+        const int d0 = quarter * 32 + (lane & ~3);      // first of the quad's dimensions
         const int nrows = min(BQ, Nq - q0);
+        float* base = dq_acc + (bh * Nq + q0) * D + d0;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (e < nrows) atomicAdd(base + size_t(e) * D, __uint_as_float(v0[e]) * scale);
-          if (e + 32 < nrows) atomicAdd(base + size_t(e + 32) * D, __uint_as_float(v1[e]) * scale);
+        for (int m = 0; m < BQ / 4; ++m) {
+          float a[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = 4 * m + j;
+            a[j] = __uint_as_float(e < 32 ? v0[e] : v1[e - 32]) * scale;
+          }
+          // bit 0: lanes i, i^1 swap the entries whose column parity differs
+          {
+            const bool odd = i4 & 1;
+            const float s0 = __shfl_xor_sync(0xffffffffu, odd ? a[0] : a[1], 1);
+            const float s1 = __shfl_xor_sync(0xffffffffu, odd ? a[2] : a[3], 1);
+            if (odd) { a[0] = s0; a[2] = s1; } else { a[1] = s0; a[3] = s1; }
+          }
+          // bit 1: lanes i, i^2 swap the entries whose column bit 1 differs
+          {
+            const bool hi = i4 & 2;
+            const float s0 = __shfl_xor_sync(0xffffffffu, hi ? a[0] : a[2], 2);
+            const float s1 = __shfl_xor_sync(0xffffffffu, hi ? a[1] : a[3], 2);
+            if (hi) { a[0] = s0; a[1] = s1; } else { a[2] = s0; a[3] = s1; }
+          }
+          // now a[k] = dQ[query 4m + i4][dimension d0 + k]
+          const int row = 4 * m + i4;
+          if (row < nrows) red_add_v4(base + size_t(row) * D, a[0], a[1], a[2], a[3]);
         }
       } else {
         // lane r = query row, columns = the d (= 64) dimensions
