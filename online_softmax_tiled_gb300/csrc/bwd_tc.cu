@@ -406,8 +406,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         uint32_t spins = 0;
         while (s < n) {
           if (t < n && t - 2 < s &&
-              mbar_try_wait(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1) &&
-              mbar_try_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1)) {
+              mbar_test_wait(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1) &&
+              mbar_test_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1)) {
             tc::fence_after_sync();
             issue_sdp(t);
             ++t;
@@ -415,7 +415,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             t_last = global_timer_ns();
             continue;
           }
-          if (mbar_try_wait(&bars.p_full[s & 1], (s >> 1) & 1)) {
+          if (mbar_test_wait(&bars.p_full[s & 1], (s >> 1) & 1)) {
             tc::fence_after_sync();
             issue_grads(s);
             ++s;
@@ -633,17 +633,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (quarter == 0 && lane == 0) {
-        for (int a = 0; a < D / 64; ++a) {
-          tma_store_3d(&map_dk, kst + a * kBK * 128, 64 * a, k0, bhkv);
-          tma_store_3d(&map_dv, vst + a * kBK * 128, 64 * a, k0, bhkv);
-        }
-        tma_store_commit_and_wait();
-      }
     } else {
       if (lane == 0) attn_flag_error(kErrTimeout);
       bars.abort = 1;
+    }
+    // Every warp of the warpgroup reaches this barrier, failed or not.
+    named_bar_sync(1, 128);
+    if (quarter == 0 && lane == 0 && !bars.abort) {
+      uint8_t* kst = smem + C::kOffK;
+      uint8_t* vst = smem + C::kOffV;
+      for (int a = 0; a < D / 64; ++a) {
+        tma_store_3d(&map_dk, kst + a * kBK * 128, 64 * a, k0, bhkv);
+        tma_store_3d(&map_dv, vst + a * kBK * 128, 64 * a, k0, bhkv);
+      }
+      tma_store_commit_and_wait();
     }
   }
 

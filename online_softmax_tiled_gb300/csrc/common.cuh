@@ -158,6 +158,17 @@ ATTN_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of phase `parity` (for loops that poll several barriers).
+ATTN_DEVINL bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`. Returns false if it ran out (or if
 // `*abort` was raised by another thread of the CTA while waiting).
 ATTN_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
