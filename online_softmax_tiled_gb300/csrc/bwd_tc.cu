@@ -94,7 +94,7 @@ struct BwdBars {
   uint64_t sdp_full[2], p_full[2];
   uint64_t ps_free[2];
   uint64_t dq_full[2], dq_free[2];
-  uint64_t dkv_full, mma_drain;
+  uint64_t dkv_full, mma_drain, mma_drain2;
   uint32_t tmem_base;
   int abort;
 };
@@ -124,6 +124,31 @@ ATTN_DEVINL uint32_t sw128_offset(int row, int col, int rows) {
   const int atom = col >> 6, c = col & 63;
   const int chunk = c >> 3;
   return uint32_t(atom * rows * 128 + row * 128 + ((chunk ^ (row & 7)) << 4) + ((c & 7) << 1));
+}
+
+// Sᵀ = K_j Q_iᵀ and dPᵀ = V_j dO_iᵀ of step s into (Sᵀ, dPᵀ) buffer s % NB
+// (all operands K-major, 128-byte swizzle), then commit to `done`.
+template <int D>
+ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* done) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  constexpr uint32_t idesc_sdp = tc::idesc_bf16_f32(kBK, BQ, false, false);
+  const int st = s % C::kQStages;
+  const int b = s % C::kSdpBufs;
+  const uint64_t k_km = tc::smem_desc(smem_u32(smem + C::kOffK), 16, 1024, tc::kLayoutSW128);
+  const uint64_t v_km = tc::smem_desc(smem_u32(smem + C::kOffV), 16, 1024, tc::kLayoutSW128);
+  const uint64_t qd = tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2) * C::kQTile), 16, 1024,
+                                    tc::kLayoutSW128);
+  const uint64_t dd = tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2 + 1) * C::kQTile), 16,
+                                    1024, tc::kLayoutSW128);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t ka = ((kk / 4) * (kBK * 128) + (kk % 4) * 32) >> 4;   // K_j / V_j
+    const uint64_t qb = ((kk / 4) * (BQ * 128) + (kk % 4) * 32) >> 4;    // Q_i / dO_i
+    tc::mma_ss(tmem + C::col_s(b), k_km + ka, qd + qb, idesc_sdp, kk > 0);
+    tc::mma_ss(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
+  }
+  tc::mma_commit(done);
 }
 
 // The (head, query tile) steps of one CTA: every query head of the group,
@@ -193,6 +218,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     mbar_init(&bars.p_full[1], 256);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.mma_drain, 1);
+    mbar_init(&bars.mma_drain2, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -292,14 +318,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     // ---------------------------------------------------------- MMA issuer
     regs_dec<120>();
     if (lane == 0) {
-      constexpr uint32_t idesc_sdp = tc::idesc_bf16_f32(kBK, BQ, false, false);
       constexpr uint32_t idesc_kv = tc::idesc_bf16_f32(kBK, D, false, true);
       constexpr uint32_t idesc_dq = C::kDqTransposed ? tc::idesc_bf16_f32(D, BQ, true, true)
                                                      : tc::idesc_bf16_f32(BQ, D, true, true);
       // Base descriptors; a descriptor's start-address field is (bytes >> 4),
       // so moving inside a tile adds (offset >> 4) to the 64-bit value.
-      const uint64_t k_km = tc::smem_desc(smem_u32(smem + C::kOffK), 16, 1024, tc::kLayoutSW128);
-      const uint64_t v_km = tc::smem_desc(smem_u32(smem + C::kOffV), 16, 1024, tc::kLayoutSW128);
       const uint64_t k_mn = tc::smem_desc(smem_u32(smem + C::kOffK), kBK * 128, 1024, tc::kLayoutSW128);
       auto q_km = [&](int st, int which) {   // Q (0) or dO (1) of a stage, K-major
         return tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2 + which) * C::kQTile), 16, 1024,
@@ -313,28 +336,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         return tc::smem_desc(smem_u32(smem + C::kOffP + pb * C::kPsTile), kBK * 128, 1024,
                              tc::kLayoutSW128);
       };
-      auto issue_sdp = [&](int s) {   // Sᵀ = K Qᵀ, dPᵀ = V dOᵀ (all operands K-major)
-        const int st = s % C::kQStages;
-        const int b = s % C::kSdpBufs;
-        const uint64_t qd = q_km(st, 0), dd = q_km(st, 1);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ka = ((kk / 4) * (kBK * 128) + (kk % 4) * 32) >> 4;   // K_j / V_j
-          const uint64_t qb = ((kk / 4) * (BQ * 128) + (kk % 4) * 32) >> 4;    // Q_i / dO_i
-          tc::mma_ss(tmem + C::col_s(b), k_km + ka, qd + qb, idesc_sdp, kk > 0);
-          tc::mma_ss(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
-        }
-        tc::mma_commit(&bars.sdp_full[b]);
-      };
+      auto issue_sdp = [&](int s) { bwd_issue_sdp<D>(smem, tmem, s, &bars.sdp_full[s % C::kSdpBufs]); };
 
-      bool ok = true;
-      if (n > 0) ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
-      for (int j = 0; j < C::kSdpBufs && j < n && ok; ++j) {
-        ok = mbar_wait_bounded(&bars.q_full[j % C::kQStages], (j / C::kQStages) & 1, abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        issue_sdp(j);
-      }
       // dV += Pᵀ dO ; dK += dSᵀ Q ; dQ(ᵀ)   for step s (after its p_full)
       auto issue_grads = [&](int s) {
         const int st = s % C::kQStages;
@@ -371,6 +374,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         tc::mma_commit(&bars.ps_free[pb]);
       };
 
+      bool ok = true;
+      if (n > 0) ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
+      if (C::kSdpBufs == 1 && n > 0 && ok) {   // the single buffer's first fill
+        ok = mbar_wait_bounded(&bars.q_full[0], 0, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_sdp(0);
+        }
+      }
       if (C::kSdpBufs == 1) {
         // One (Sᵀ, dPᵀ) buffer, which also holds Pᵀ, dSᵀ of the step: the
         // gradients of step s are issued first, then the buffer is refilled
@@ -395,39 +407,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           }
         }
       } else {
-        // Two buffers: a greedy issuer. tcgen05.mma issue stalls once the
-        // tensor pipe's queue is full, so the thread must never sit on one
-        // barrier while other work is ready. Work items: Sᵀ/dPᵀ of step t
-        // (buffer t & 1 drained of dQᵀ(t-2), Q/dO(t) loaded) and the
-        // gradients of step s (its softmax done). Sᵀ/dPᵀ first: it feeds the
-        // softmax warpgroups.
-        int s = 0, t = min(C::kSdpBufs, n);
-        uint64_t t_last = global_timer_ns();   // bounded: no progress for the wait limit = abort
-        uint32_t spins = 0;
-        while (s < n) {
-          if (t < n && t - 2 < s &&
-              mbar_test_wait(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1) &&
-              mbar_test_wait(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1)) {
-            tc::fence_after_sync();
-            issue_sdp(t);
-            ++t;
-            spins = 0;
-            t_last = global_timer_ns();
-            continue;
-          }
-          if (mbar_test_wait(&bars.p_full[s & 1], (s >> 1) & 1)) {
-            tc::fence_after_sync();
-            issue_grads(s);
-            ++s;
-            spins = 0;
-            t_last = global_timer_ns();
-            continue;
-          }
-          if ((++spins & 255u) == 0 &&
-              (*abort_flag || global_timer_ns() - t_last > kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
+        // Two buffers: this thread issues the gradient MMAs of every step
+        // (after its softmax); warp 3 issues Sᵀ/dPᵀ (see below). tcgen05.mma
+        // issue returns only as the tensor pipe accepts the instruction, so
+        // one thread serving both streams would sit on one barrier while the
+        // other stream's work is ready.
+        for (int s = 0; s < n && ok; ++s) {
+          ok = mbar_wait_bounded(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_grads(s);
         }
       }
       if (!ok) {
@@ -439,7 +428,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       mbar_wait_bounded(&bars.mma_drain, 0, nullptr);
     }
   } else if (warp == 3) {
-    regs_dec<120>();                                    // idle warp of the first warpgroup
+    // ---------------------------------------------------------- Sᵀ/dPᵀ issuer (d = 128)
+    regs_dec<120>();
+    if (C::kSdpBufs == 2 && lane == 0 && n > 0) {
+      bool ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
+      for (int t = 0; t < n && ok; ++t) {
+        // buffer t & 1 must be drained of dQᵀ(t-2); Q/dO(t) loaded
+        if (t >= 2) ok = mbar_wait_bounded(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1, abort_flag);
+        if (ok) ok = mbar_wait_bounded(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1,
+                                       abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        bwd_issue_sdp<D>(smem, tmem, t, &bars.sdp_full[t & 1]);
+      }
+      if (!ok) {
+        attn_flag_error(kErrTimeout);
+        bars.abort = 1;
+      }
+      tc::mma_commit(&bars.mma_drain2);
+      mbar_wait_bounded(&bars.mma_drain2, 0, nullptr);
+    }
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroups
     // Two warpgroups share the key rows (TMEM lanes) and split the BQ query
