@@ -113,6 +113,9 @@ ATTN_DEVINL void tma_store_commit_and_wait() {
 ATTN_DEVINL void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+ATTN_DEVINL void red_add_f32(float* addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
 ATTN_DEVINL void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
                "f"(c), "f"(d) : "memory");
@@ -127,7 +130,8 @@ ATTN_DEVINL uint32_t sw128_offset(int row, int col, int rows) {
 }
 
 // Sᵀ = K_j Q_iᵀ and dPᵀ = V_j dO_iᵀ of step s into (Sᵀ, dPᵀ) buffer s % NB
-// (all operands K-major, 128-byte swizzle), then commit to `done`.
+// (all operands K-major, 128-byte swizzle), then commit to `done`. Called by
+// all lanes of the issuing warp.
 template <int D>
 ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* done) {
   using C = BwdCfg<D>;
@@ -145,10 +149,10 @@ ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* do
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t ka = ((kk / 4) * (kBK * 128) + (kk % 4) * 32) >> 4;   // K_j / V_j
     const uint64_t qb = ((kk / 4) * (BQ * 128) + (kk % 4) * 32) >> 4;    // Q_i / dO_i
-    tc::mma_ss(tmem + C::col_s(b), k_km + ka, qd + qb, idesc_sdp, kk > 0);
-    tc::mma_ss(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
+    tc::mma_ss_warp(tmem + C::col_s(b), k_km + ka, qd + qb, idesc_sdp, kk > 0);
+    tc::mma_ss_warp(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
   }
-  tc::mma_commit(done);
+  tc::mma_commit_warp(done);
 }
 
 // The (head, query tile) steps of one CTA: every query head of the group,
@@ -316,8 +320,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs this loop; one elected lane issues each MMA.
     regs_dec<120>();
-    if (lane == 0) {
+    {
       constexpr uint32_t idesc_kv = tc::idesc_bf16_f32(kBK, D, false, true);
       constexpr uint32_t idesc_dq = C::kDqTransposed ? tc::idesc_bf16_f32(D, BQ, true, true)
                                                      : tc::idesc_bf16_f32(BQ, D, true, true);
@@ -352,11 +357,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             const uint32_t ac = C::col_pair(kk * 16);
             const uint64_t step = uint64_t(kk * 2048) >> 4;                      // 16 query rows
             const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-            tc::mma_ts(tmem + C::kColDV, tmem + C::col_s(b) + ac, dob + step, idesc_kv, acc);
-            tc::mma_ts(tmem + C::kColDK, tmem + C::col_dp(b) + ac, qb + step, idesc_kv, acc);
+            tc::mma_ts_warp(tmem + C::kColDV, tmem + C::col_s(b) + ac, dob + step, idesc_kv, acc);
+            tc::mma_ts_warp(tmem + C::kColDK, tmem + C::col_dp(b) + ac, qb + step, idesc_kv, acc);
           }
         }
-        tc::mma_commit(&bars.q_empty[st]);           // Q_i, dO_i, LSE, D of the stage consumed
+        tc::mma_commit_warp(&bars.q_empty[st]);      // Q_i, dO_i, LSE, D of the stage consumed
         {
           // dQᵀ = K_jᵀ dSᵀ (A = K_j MN-major over d atoms, B = dSᵀ) for d = 128;
           // dQ = dS K_j (A = dSᵀ MN-major over query atoms, B = K_j) for d = 64.
@@ -367,17 +372,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t step = uint64_t(kk * 2048) >> 4;   // 16 keys down both operands
-            tc::mma_ss(tmem + dq_col, a0 + step, b0 + step, idesc_dq, kk > 0);
+            tc::mma_ss_warp(tmem + dq_col, a0 + step, b0 + step, idesc_dq, kk > 0);
           }
         }
-        tc::mma_commit(&bars.dq_full[db]);
-        tc::mma_commit(&bars.ps_free[pb]);
+        tc::mma_commit_warp(&bars.dq_full[db]);
+        tc::mma_commit_warp(&bars.ps_free[pb]);
       };
 
       bool ok = true;
-      if (n > 0) ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
+      if (n > 0) ok = mbar_wait_warp(&bars.kv_full, 0, abort_flag);
       if (C::kSdpBufs == 1 && n > 0 && ok) {   // the single buffer's first fill
-        ok = mbar_wait_bounded(&bars.q_full[0], 0, abort_flag);
+        ok = mbar_wait_warp(&bars.q_full[0], 0, abort_flag);
         if (ok) {
           tc::fence_after_sync();
           issue_sdp(0);
@@ -388,19 +393,19 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         // gradients of step s are issued first, then the buffer is refilled
         // with step s+1 (the tensor pipe executes in issue order).
         for (int s = 0; s < n && ok; ++s) {
-          ok = mbar_wait_bounded(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
+          ok = mbar_wait_warp(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
           if (s >= 2) {   // dQ TMEM buffer s & 1 drained (step s-2)
-            ok = mbar_wait_bounded(&bars.dq_free[s & 1], ((s >> 1) - 1) & 1, abort_flag);
+            ok = mbar_wait_warp(&bars.dq_free[s & 1], ((s >> 1) - 1) & 1, abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
           }
           issue_grads(s);
           if (s + 1 < n) {
             const int s1 = s + 1;
-            ok = mbar_wait_bounded(&bars.q_full[s1 % C::kQStages], (s1 / C::kQStages) & 1,
-                                   abort_flag);
+            ok = mbar_wait_warp(&bars.q_full[s1 % C::kQStages], (s1 / C::kQStages) & 1,
+                                abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
             issue_sdp(s1);
@@ -413,40 +418,43 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         // one thread serving both streams would sit on one barrier while the
         // other stream's work is ready.
         for (int s = 0; s < n && ok; ++s) {
-          ok = mbar_wait_bounded(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
+          ok = mbar_wait_warp(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
           issue_grads(s);
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         attn_flag_error(kErrTimeout);
         bars.abort = 1;
       }
-      tc::mma_commit(&bars.dkv_full);
-      tc::mma_commit(&bars.mma_drain);
-      mbar_wait_bounded(&bars.mma_drain, 0, nullptr);
+      __syncwarp();
+      tc::mma_commit_warp(&bars.dkv_full);
+      tc::mma_commit_warp(&bars.mma_drain);
+      mbar_wait_warp(&bars.mma_drain, 0, nullptr);
     }
   } else if (warp == 3) {
     // ---------------------------------------------------------- Sᵀ/dPᵀ issuer (d = 128)
+    // The whole warp runs this loop; one elected lane issues each MMA.
     regs_dec<120>();
-    if (C::kSdpBufs == 2 && lane == 0 && n > 0) {
-      bool ok = mbar_wait_bounded(&bars.kv_full, 0, abort_flag);
+    if (C::kSdpBufs == 2 && n > 0) {
+      bool ok = mbar_wait_warp(&bars.kv_full, 0, abort_flag);
       for (int t = 0; t < n && ok; ++t) {
         // buffer t & 1 must be drained of dQᵀ(t-2); Q/dO(t) loaded
-        if (t >= 2) ok = mbar_wait_bounded(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1, abort_flag);
-        if (ok) ok = mbar_wait_bounded(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1,
-                                       abort_flag);
+        if (t >= 2) ok = mbar_wait_warp(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1, abort_flag);
+        if (ok) ok = mbar_wait_warp(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1,
+                                    abort_flag);
         if (!ok) break;
         tc::fence_after_sync();
         bwd_issue_sdp<D>(smem, tmem, t, &bars.sdp_full[t & 1]);
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         attn_flag_error(kErrTimeout);
         bars.abort = 1;
       }
-      tc::mma_commit(&bars.mma_drain2);
-      mbar_wait_bounded(&bars.mma_drain2, 0, nullptr);
+      __syncwarp();
+      tc::mma_commit_warp(&bars.mma_drain2);
+      mbar_wait_warp(&bars.mma_drain2, 0, nullptr);
     }
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroups
@@ -559,40 +567,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tc::fence_before_sync();
       mbar_arrive(&bars.dq_free[db]);
       if (C::kDqTransposed) {
-        // lane r = dimension, columns = the BQ (= 64) query rows of the step.
-        // A 4x4 transpose inside each quad of lanes gives every lane four
-        // consecutive dimensions of one query row, added into the float32
-        // accumulator with one 16-byte reduction: 16 per lane per step.
-        const int i4 = lane & 3;
-        const int d0 = quarter * 32 + (lane & ~3);      // first of the quad's dimensions
+        // lane r = dimension, columns = the BQ (= 64) query rows of the step:
+        // one 4-byte reduction per (query, dimension); the 32 lanes of a warp
+        // cover 32 consecutive dimensions of one query row (128 bytes). No
+        // shuffles or selects: the integer pipe stays free for the tensor
+        // core's instruction stream.
         const int nrows = min(BQ, Nq - q0);
-        float* base = dq_acc + (bh * Nq + q0) * D + d0;
+        float* base = dq_acc + (bh * Nq + q0) * D + r;
 #pragma unroll
-        for (int m = 0; m < BQ / 4; ++m) {
-          float a[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int e = 4 * m + j;
-            a[j] = __uint_as_float(e < 32 ? v0[e] : v1[e - 32]) * scale;
-          }
-          // bit 0: lanes i, i^1 swap the entries whose column parity differs
-          {
-            const bool odd = i4 & 1;
-            const float s0 = __shfl_xor_sync(0xffffffffu, odd ? a[0] : a[1], 1);
-            const float s1 = __shfl_xor_sync(0xffffffffu, odd ? a[2] : a[3], 1);
-            if (odd) { a[0] = s0; a[2] = s1; } else { a[1] = s0; a[3] = s1; }
-          }
-          // bit 1: lanes i, i^2 swap the entries whose column bit 1 differs
-          {
-            const bool hi = i4 & 2;
-            const float s0 = __shfl_xor_sync(0xffffffffu, hi ? a[0] : a[2], 2);
-            const float s1 = __shfl_xor_sync(0xffffffffu, hi ? a[1] : a[3], 2);
-            if (hi) { a[0] = s0; a[1] = s1; } else { a[2] = s0; a[3] = s1; }
-          }
-          // now a[k] = dQ[query 4m + i4][dimension d0 + k]
-          const int row = 4 * m + i4;
-          if (row < nrows) red_add_v4(base + size_t(row) * D, a[0], a[1], a[2], a[3]);
-        }
+        for (int e = 0; e < BQ; ++e)
+          if (e < nrows) red_add_f32(base + size_t(e) * D, __uint_as_float(e < 32 ? v0[e] : v1[e - 32]) * scale);
       } else {
         // lane r = query row, columns = the d (= 64) dimensions
         if (q0 + r < Nq) {

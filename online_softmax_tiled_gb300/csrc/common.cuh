@@ -183,6 +183,12 @@ ATTN_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int*
   }
 }
 
+// The same wait made by every lane of a converged warp; the result is the
+// AND over the lanes, so the warp stays converged after it.
+ATTN_DEVINL bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
+}
+
 // ----------------------------------------------------------------------------
 // Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.
 // Both addresses 16-byte aligned, size a multiple of 16.

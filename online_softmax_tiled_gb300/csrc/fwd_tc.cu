@@ -222,14 +222,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
   } else if (C::kSeparateP && (warp == 1 || warp == 2)) {
     // ------------------------------------------------------------ MMA issuers (d = 64)
-    // One issuing thread per query tile. tcgen05.mma issue only returns as
-    // the tensor pipe accepts the instruction (its queue is shallow), so a
-    // single thread waiting on one tile's barrier would starve the pipe even
-    // when the other tile's work is ready.
+    // One issuing warp per query tile (each runs its loop converged; one
+    // elected lane issues). tcgen05.mma issue only returns as the tensor pipe
+    // accepts the instruction (its queue is shallow), so a single issuer
+    // waiting on one tile's barrier would starve the pipe even when the other
+    // tile's work is ready.
     regs_dec<80>();
     const int t = warp - 1;
     const int n = n_t[t], n_other = n_t[t ^ 1];
-    if (lane == 0 && nj > 0) {
+    if (nj > 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, false, true);
       const uint32_t s_col = t == 0 ? C::kColS0 : C::kColS1;
@@ -243,36 +244,37 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       // other tile does not visit index j this thread releases twice (the
       // plain arrival, the commit only once its MMAs have read the stage).
       auto release = [&](uint64_t* bar, int j) {
-        tc::mma_commit(bar);
-        if (j >= n_other) mbar_arrive(bar);
+        tc::mma_commit_warp(bar);
+        if (j >= n_other && lane == 0) mbar_arrive(bar);
+        __syncwarp();
       };
       auto issue_s = [&](int j) {
         const uint32_t ka = k_base + (j % C::kStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-          tc::mma_ss(tmem + s_col, tc::smem_desc(qa + off, 16, 1024, tc::kLayoutSW128),
-                     tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
+          tc::mma_ss_warp(tmem + s_col, tc::smem_desc(qa + off, 16, 1024, tc::kLayoutSW128),
+                          tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
         }
-        tc::mma_commit(&bars.s_full[t]);
+        tc::mma_commit_warp(&bars.s_full[t]);
         release(&bars.k_empty[j % C::kStages], j);
       };
       auto issue_pv = [&](int j) {
         const uint32_t va = v_base + (j % C::kStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          tc::mma_ts(tmem + o_col, tmem + p_col + kk * 8,
-                     tc::smem_desc(va + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128), idesc_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_ts_warp(tmem + o_col, tmem + p_col + kk * 8,
+                          tc::smem_desc(va + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128), idesc_o,
+                          (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&bars.o_done[t]);
+        tc::mma_commit_warp(&bars.o_done[t]);
         release(&bars.v_empty[j % C::kStages], j);
       };
 
       bool ok = true;
       if (n > 0) {
-        ok = mbar_wait_bounded(&bars.q_full, 0, abort_flag);
-        if (ok) ok = mbar_wait_bounded(&bars.k_full[0], 0, abort_flag);
+        ok = mbar_wait_warp(&bars.q_full, 0, abort_flag);
+        if (ok) ok = mbar_wait_warp(&bars.k_full[0], 0, abort_flag);
         if (ok) {
           tc::fence_after_sync();
           issue_s(0);
@@ -282,38 +284,40 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const int j1 = j + 1;
         if (C::kSeparateP && j1 < n) {
           // S_t(j+1) as soon as the softmax has read S_t(j) and K_{j+1} is in
-          ok = mbar_wait_bounded(&bars.s_free[t], j & 1, abort_flag);
-          if (ok) ok = mbar_wait_bounded(&bars.k_full[j1 % C::kStages], (j1 / C::kStages) & 1,
-                                         abort_flag);
+          ok = mbar_wait_warp(&bars.s_free[t], j & 1, abort_flag);
+          if (ok) ok = mbar_wait_warp(&bars.k_full[j1 % C::kStages], (j1 / C::kStages) & 1,
+                                      abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
           issue_s(j1);
         }
-        ok = mbar_wait_bounded(&bars.v_full[j % C::kStages], (j / C::kStages) & 1, abort_flag);
-        if (ok) ok = mbar_wait_bounded(&bars.p_full[t], j & 1, abort_flag);
+        ok = mbar_wait_warp(&bars.v_full[j % C::kStages], (j / C::kStages) & 1, abort_flag);
+        if (ok) ok = mbar_wait_warp(&bars.p_full[t], j & 1, abort_flag);
         if (!ok) break;
         tc::fence_after_sync();
         issue_pv(j);
         if (!C::kSeparateP && j1 < n) {
           // P̃_t(j) lives in the S_t columns: S_t(j+1) after PV_t(j) (issue order)
-          ok = mbar_wait_bounded(&bars.k_full[j1 % C::kStages], (j1 / C::kStages) & 1, abort_flag);
+          ok = mbar_wait_warp(&bars.k_full[j1 % C::kStages], (j1 / C::kStages) & 1, abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
           issue_s(j1);
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         attn_flag_error(kErrTimeout);
         bars.abort = 1;
       }
-      // Drain: every MMA this thread issued has completed before TMEM is freed.
-      tc::mma_commit(&bars.mma_drain[t]);
-      mbar_wait_bounded(&bars.mma_drain[t], 0, nullptr);
+      __syncwarp();
+      // Drain: every MMA this warp issued has completed before TMEM is freed.
+      tc::mma_commit_warp(&bars.mma_drain[t]);
+      mbar_wait_warp(&bars.mma_drain[t], 0, nullptr);
     }
   } else if (!C::kSeparateP && warp == 1) {
     // ------------------------------------------------------------ MMA issuer (d = 128)
+    // The whole warp runs this loop; one elected lane issues each MMA.
     regs_dec<80>();
-    if (lane == 0 && nj > 0) {
+    if (nj > 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, false, true);
       const uint32_t s_col[2] = {C::kColS0, C::kColS1};
@@ -328,39 +332,39 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-          tc::mma_ss(tmem + s_col[t], tc::smem_desc(qa + off, 16, 1024, tc::kLayoutSW128),
-                     tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
+          tc::mma_ss_warp(tmem + s_col[t], tc::smem_desc(qa + off, 16, 1024, tc::kLayoutSW128),
+                          tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
         }
-        tc::mma_commit(&bars.s_full[t]);
+        tc::mma_commit_warp(&bars.s_full[t]);
       };
       auto issue_pv = [&](int t, int j) {
         const uint32_t va = v_base + (j % C::kStages) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          tc::mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8,
-                     tc::smem_desc(va + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128), idesc_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_ts_warp(tmem + o_col[t], tmem + s_col[t] + kk * 8,
+                          tc::smem_desc(va + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128), idesc_o,
+                          (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&bars.o_done[t]);
+        tc::mma_commit_warp(&bars.o_done[t]);
       };
 
-      bool ok = mbar_wait_bounded(&bars.q_full, 0, abort_flag);
-      if (ok) ok = mbar_wait_bounded(&bars.k_full[0], 0, abort_flag);
+      bool ok = mbar_wait_warp(&bars.q_full, 0, abort_flag);
+      if (ok) ok = mbar_wait_warp(&bars.k_full[0], 0, abort_flag);
       if (ok) {
         tc::fence_after_sync();
         for (int t = 0; t < 2; ++t)
           if (n_t[t] > 0) issue_s(t, 0);
-        tc::mma_commit(&bars.k_empty[0]);
+        tc::mma_commit_warp(&bars.k_empty[0]);
       }
       for (int j = 0; j < nj && ok; ++j) {
         const bool has_next = j + 1 < nj;
-        ok = mbar_wait_bounded(&bars.v_full[j % C::kStages], (j / C::kStages) & 1, abort_flag);
+        ok = mbar_wait_warp(&bars.v_full[j % C::kStages], (j / C::kStages) & 1, abort_flag);
         if (ok && has_next)
-          ok = mbar_wait_bounded(&bars.k_full[(j + 1) % C::kStages],
-                                 ((j + 1) / C::kStages) & 1, abort_flag);
+          ok = mbar_wait_warp(&bars.k_full[(j + 1) % C::kStages], ((j + 1) / C::kStages) & 1,
+                              abort_flag);
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < n_t[t]) {
-            ok = mbar_wait_bounded(&bars.p_full[t], j & 1, abort_flag);
+            ok = mbar_wait_warp(&bars.p_full[t], j & 1, abort_flag);
             if (!ok) break;
             tc::fence_after_sync();
             issue_pv(t, j);
@@ -368,16 +372,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           if (has_next && j + 1 < n_t[t]) issue_s(t, j + 1);
         }
         if (!ok) break;
-        tc::mma_commit(&bars.v_empty[j % C::kStages]);
-        if (has_next) tc::mma_commit(&bars.k_empty[(j + 1) % C::kStages]);
+        tc::mma_commit_warp(&bars.v_empty[j % C::kStages]);
+        if (has_next) tc::mma_commit_warp(&bars.k_empty[(j + 1) % C::kStages]);
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         attn_flag_error(kErrTimeout);
         bars.abort = 1;
       }
-      // Drain: every MMA this thread issued has completed before TMEM is freed.
-      tc::mma_commit(&bars.mma_drain[0]);
-      mbar_wait_bounded(&bars.mma_drain[0], 0, nullptr);
+      __syncwarp();
+      // Drain: every MMA this warp issued has completed before TMEM is freed.
+      tc::mma_commit_warp(&bars.mma_drain[0]);
+      mbar_wait_warp(&bars.mma_drain[0], 0, nullptr);
     }
   } else if (warp < 4) {
     regs_dec<80>();                                // idle warp of the first warpgroup

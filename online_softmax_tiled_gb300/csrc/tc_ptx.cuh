@@ -63,6 +63,34 @@ ATTN_DEVINL void mma_commit(uint64_t* bar) {
       ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Warp-collective forms of the three calls above: all 32 lanes of a
+// converged warp make the call with the same operands and elect.sync picks
+// the one lane that issues (the same lane every time, so its commits track
+// its MMAs). Keeping the issuing warp converged lets the compiler keep the
+// operands in the uniform datapath; measured on GB300, MMAs issued from a
+// lone divergent thread ran up to 1.8x slower whenever the other warps of
+// its SM sub-partition kept the integer pipe busy, and these did not.
+ATTN_DEVINL void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+ATTN_DEVINL void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+ATTN_DEVINL void mma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Instruction descriptor for kind::f16: D float32, A and B bf16, dense.
 // Bits: [4,6) D format (1 = f32); [7,10) A format (1 = bf16); [10,13) B
 // format; 15 A major (0 = K-major, 1 = MN-major); 16 B major; [17,23) N>>3;
