@@ -62,7 +62,11 @@ struct BwdCfg {
   static constexpr int kOffQ = kOffV + kKVTile;                      // [stage] Q, dO
   static constexpr int kOffP = kOffQ + kQStages * 2 * kQTile;       // [buf] dSᵀ
   static constexpr int kOffVec = kOffP + kPsBufs * kPsTile;         // [stage] -LSE·log2e, -D
-  static constexpr int kSmemBytes = kOffVec + kQStages * 2 * BQ * 4;
+  // d = 128: dQ of one step staged row-major in float32 for the bulk
+  // reduction into the accumulator (128-byte aligned is enough unswizzled)
+  static constexpr int kOffDq = kOffVec + kQStages * 2 * BQ * 4;
+  static constexpr int kDqStageBytes = kDqTransposed ? BQ * D * 4 : 0;
+  static constexpr int kSmemBytes = kOffDq + kDqStageBytes;
   static constexpr int kDynSmem = kSmemBytes + 1024;
   // tensor memory columns. d = 128: two (Sᵀ, dPᵀ) buffers of 64 + 64
   // columns; dQᵀ(s) is written over the Sᵀ columns of its own buffer once the
@@ -85,7 +89,8 @@ struct BwdCfg {
   __host__ __device__ static constexpr uint32_t col_pair(int q0) {
     return (q0 / CW) * CW + (q0 % CW) / 2;
   }
-  static_assert(kDynSmem <= 232448, "shared-memory budget");
+  static_assert(kOffDq % 128 == 0, "bulk-copy source alignment");
+  static_assert(kDynSmem + 256 <= 232448, "shared-memory budget (dynamic + static)");
 };
 
 struct BwdBars {
@@ -113,8 +118,29 @@ ATTN_DEVINL void tma_store_commit_and_wait() {
 ATTN_DEVINL void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-ATTN_DEVINL void red_add_f32(float* addr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+// Bulk tensor reduction: add the shared-memory box at `smem_src` into the
+// float32 tensor of `map` at coordinates (c0, c1, c2).
+ATTN_DEVINL void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
+                                   int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+ATTN_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+ATTN_DEVINL void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+ATTN_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Named barrier over `count` threads that also ANDs `pred` across them.
+ATTN_DEVINL bool named_bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(uint32_t(pred)), "r"(id), "r"(count) : "memory");
+  return r != 0;
 }
 ATTN_DEVINL void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
@@ -178,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
-              const float* __restrict__ lse, const float* __restrict__ row_term,
+              const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse, const float* __restrict__ row_term,
               float* __restrict__ dq_acc, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
               int n_ktiles) {
   using C = BwdCfg<D>;
@@ -547,6 +573,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    // d = 128: the dQᵀ tile (lane = dimension) is scaled, written row-major
+    // into the float32 staging buffer and added into the accumulator with one
+    // bulk tensor reduction per step (the tensor memory is released right
+    // after the load). d = 64: lane = query row, 16-byte reductions per row.
+    const bool bulk_issuer = quarter == 0 && lane == 0;
+    float* stage = reinterpret_cast<float*>(smem + C::kOffDq);
     bool ok = true;
     for (int s = 0; s < n; ++s) {
       const int db = s & 1;
@@ -554,10 +586,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       plan.at(s, hh, qt);
       const size_t bh = size_t(b) * Hq + g * group + hh;
       const int q0 = qt * BQ;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars.dq_full[db], (s >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
+      const bool got = mbar_wait_bounded(&bars.dq_full[db], (s >> 1) & 1, abort_flag);
+      // The whole warpgroup agrees on the outcome (its barriers below need all
+      // 128 threads); for d = 128 this barrier also tells every thread that the
+      // bulk reduction of step s-1 has finished reading the staging buffer.
+      ok = C::kDqTransposed ? named_bar_and(1, 128, got) : __all_sync(0xffffffffu, got);
+      if (!ok) break;
       tc::fence_after_sync();
       const uint32_t col0 = C::kDqInS ? C::col_s(s % C::kSdpBufs) : C::kColDQ + db * C::kDqCols;
       uint32_t v0[32], v1[32];
@@ -567,16 +601,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tc::fence_before_sync();
       mbar_arrive(&bars.dq_free[db]);
       if (C::kDqTransposed) {
-        // lane r = dimension, columns = the BQ (= 64) query rows of the step:
-        // one 4-byte reduction per (query, dimension); the 32 lanes of a warp
-        // cover 32 consecutive dimensions of one query row (128 bytes). No
-        // shuffles or selects: the integer pipe stays free for the tensor
-        // core's instruction stream.
-        const int nrows = min(BQ, Nq - q0);
-        float* base = dq_acc + (bh * Nq + q0) * D + r;
+        // stage[q][d]: for each query a warp writes 32 consecutive floats
 #pragma unroll
         for (int e = 0; e < BQ; ++e)
-          if (e < nrows) red_add_f32(base + size_t(e) * D, __uint_as_float(e < 32 ? v0[e] : v1[e - 32]) * scale);
+          stage[e * D + r] = __uint_as_float(e < 32 ? v0[e] : v1[e - 32]) * scale;
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (bulk_issuer) {
+          // rows past Nq fall outside the map and are not written
+          tma_reduce_add_3d(&map_dq, stage, 0, q0, int(bh));
+          bulk_commit();
+          bulk_wait_read_all();
+        }
       } else {
         // lane r = query row, columns = the d (= 64) dimensions
         if (q0 + r < Nq) {
@@ -592,6 +628,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
       }
     }
+    // every bulk reduction of this CTA has landed before it exits
+    if (C::kDqTransposed && bulk_issuer) bulk_wait_all();
     // dK = scale·(dSᵀ Q summed), dV = Pᵀ dO summed -> bf16 -> K_j / V_j tiles -> TMA store.
     if (ok && n > 0)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.dkv_full, 0, abort_flag));
@@ -653,7 +691,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 template <int D>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
   const uint64_t bhq = uint64_t(a.B) * a.Hq, bhk = uint64_t(a.B) * a.Hkv;
   if (!make_map_bf16_3d(&mq, a.q, D, a.Nq, bhq, C::BQ) ||
       !make_map_bf16_3d(&mdo, a.dO, D, a.Nq, bhq, C::BQ) ||
@@ -662,6 +700,11 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
       !make_map_bf16_3d(&mdk, a.dk, D, a.Nk, bhk, kBK) ||
       !make_map_bf16_3d(&mdv, a.dv, D, a.Nk, bhk, kBK))
     return cudaErrorInvalidValue;
+  if (C::kDqTransposed) {
+    if (!make_map_f32_3d(&mdq, a.dq_acc, D, a.Nq, bhq, D, C::BQ)) return cudaErrorInvalidValue;
+  } else {
+    mdq = mq;   // unused: d = 64 adds dQ with per-row reductions
+  }
   cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
@@ -669,7 +712,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   const long blocks = long(n_ktiles) * a.B * a.Hkv;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
   bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
-      mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale,
+      mq, mk, mv, mdo, mdk, mdv, mdq, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale,
       a.causal, n_ktiles);
   return cudaGetLastError();
 }

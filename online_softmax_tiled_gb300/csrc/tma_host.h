@@ -46,4 +46,21 @@ inline bool make_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over a float32 tensor viewed as [outer][rows][cols] (cols contiguous),
+// box = (box_cols, box_rows, 1), no swizzle: the shared-memory side of a copy
+// is the plain row-major box. Used for bulk reductions into an accumulator;
+// rows >= `rows` of a box are left untouched.
+inline bool make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                            uint64_t outer, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, outer};
+  const cuuint64_t strides[2] = {cols * 4, rows * cols * 4};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace attn
