@@ -450,32 +450,46 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // With its own P̃ columns, P̃_t(j) may only be written once PV_t(j-1)
-      // has read P̃_t(j-1); the same wait covers the Õ rescale below.
-      bool pv_prev_done = false;
-      if (C::kSeparateP && j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.o_done[t], (j - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc::fence_after_sync();
-        pv_prev_done = true;
-      }
-
       // P̃ = exp2(s·c - m_ref) -> bf16 pairs (over the first 64 score columns,
       // or into the tile's own P̃ columns).
       const f2 cc2{c, c}, nm2{neg_m, neg_m};
       f2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // 4 independent sums
+      bool pv_prev_done = false;
+      if (C::kSeparateP) {
+        // With its own P̃ columns, P̃_t(j) may only be written once PV_t(j-1)
+        // has read P̃_t(j-1): all 128 exponentials are computed first, so the
+        // wait overlaps the special-function work instead of preceding it.
+        uint32_t pk[64];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          f2 x = fma2(f2{s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]}, cc2, nm2);
+        for (int e = 0; e < 64; ++e) {
+          f2 x = fma2(f2{s[2 * e], s[2 * e + 1]}, cc2, nm2);
           x.x = fast_exp2(x.x);
           x.y = fast_exp2(x.y);
           rs2[e & 3] = add2(rs2[e & 3], x);
           pk[e] = pack_bf16x2(x.x, x.y);
         }
-        tmem_st32(p_addr + half * 32, pk);
+        if (j > 0) {   // the same wait covers the Õ rescale below
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.o_done[t], (j - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc::fence_after_sync();
+          pv_prev_done = true;
+        }
+        tmem_st32(p_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(p_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            f2 x = fma2(f2{s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]}, cc2, nm2);
+            x.x = fast_exp2(x.x);
+            x.y = fast_exp2(x.y);
+            rs2[e & 3] = add2(rs2[e & 3], x);
+            pk[e] = pack_bf16x2(x.x, x.y);
+          }
+          tmem_st32(p_addr + half * 32, pk);
+        }
       }
       const f2 rsa = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
       const float rs = rsa.x + rsa.y;
