@@ -276,11 +276,15 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 }
 
 // One warp per output row; lane owns float4 column groups lane, lane+32, ...
+// The partials of a row are fetched eight at a time with independent loads
+// (their weights exp(m_t - m) are computed once per lane first), so a row
+// costs about S/8 memory round trips rather than S.
 template <typename TOut>
 __global__ void __launch_bounds__(256)
 merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
              const float* __restrict__ l_part, TOut* __restrict__ o, float* __restrict__ lse,
              int rows, int S, int d) {
+  constexpr int kBatch = 8;
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -290,6 +294,7 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
   for (int t = lane; t < S; t += 32) mx = fmaxf(mx, mr[t]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  // lane t (< S) holds the weight of partial t; rows with S > 32 loop
   float l = 0.f;
   if (mx != -INFINITY)
     for (int t = lane; t < S; t += 32) {
@@ -300,18 +305,28 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
   for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   const bool empty = !(l > 0.f);
   const float inv = empty ? 0.f : 1.f / l;
-  for (int c4 = lane; c4 < d / 4; c4 += 32) {
+  const float4* prow = reinterpret_cast<const float4*>(o_part + size_t(row) * S * d);
+  const int d4 = d / 4;
+  for (int c4 = lane; c4 < d4; c4 += 32) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!empty)
-      for (int t = 0; t < S; ++t) {
-        const float mt = mr[t];
-        if (mt == -INFINITY) continue;
-        const float w = expf(mt - mx);
-        const float4 x = reinterpret_cast<const float4*>(o_part + (size_t(row) * S + t) * d)[c4];
-        acc.x = fmaf(w, x.x, acc.x);
-        acc.y = fmaf(w, x.y, acc.y);
-        acc.z = fmaf(w, x.z, acc.z);
-        acc.w = fmaf(w, x.w, acc.w);
+      for (int t0 = 0; t0 < S; t0 += kBatch) {
+        float4 x[kBatch];
+        float w[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int t = t0 + u;
+          const float mt = t < S ? mr[t] : -INFINITY;
+          w[u] = mt == -INFINITY ? 0.f : expf(mt - mx);
+          x[u] = w[u] != 0.f ? prow[size_t(t) * d4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          acc.x = fmaf(w[u], x[u].x, acc.x);
+          acc.y = fmaf(w[u], x[u].y, acc.y);
+          acc.z = fmaf(w[u], x[u].z, acc.z);
+          acc.w = fmaf(w[u], x[u].w, acc.w);
+        }
       }
     TOut* orow = o + size_t(row) * d + 4 * c4;
     orow[0] = from_f32<TOut>(acc.x * inv);
