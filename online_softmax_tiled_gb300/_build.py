@@ -24,7 +24,7 @@ LIB_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libattn_gb300.so")
 
 SOURCES = ["api.cu", "fwd_simt.cu", "fwd_tc.cu", "bwd_aux.cu", "bwd_simt.cu", "bwd_tc.cu",
-           "decode.cu"]
+           "bwd_dq.cu", "decode.cu"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

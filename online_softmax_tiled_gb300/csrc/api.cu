@@ -112,9 +112,19 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   char* ws = static_cast<char*>(workspace);
   BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, dt,
             reinterpret_cast<float*>(ws + lay.row_term), reinterpret_cast<float*>(ws + lay.dq_acc),
-            static_cast<cudaStream_t>(stream)};
+            static_cast<cudaStream_t>(stream), true};
+  // bf16, d = 128: a key-tile pass (dK, dV) and a query-tile pass (dQ, written
+  // in bf16 directly; the float32 accumulator is not used). Otherwise one
+  // pass adds dQ into the float32 accumulator, converted at the end.
+  const bool split_dq = dt == ATTN_BF16 && d == 128;
+  a.zero_dq_acc = !split_dq;
   cudaError_t e = launch_bwd_preprocess(a);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (split_dq) {
+    e = launch_bwd_tc(a);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    return from_cuda(launch_bwd_dq(a));
+  }
   e = (dt == ATTN_BF16) ? launch_bwd_tc(a) : launch_bwd_simt(a);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return from_cuda(launch_bwd_convert(a));
@@ -169,7 +179,8 @@ attn_status attn_merge_partials(const float* o_part, const float* m_part, const 
 attn_status attn_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  const uint32_t w = take_error_fwd_tc() | take_error_bwd_tc() | take_error_decode();
+  const uint32_t w =
+      take_error_fwd_tc() | take_error_bwd_tc() | take_error_bwd_dq() | take_error_decode();
   if (w == 0xffffffffu) return ATTN_ERR_CUDA;
   if (w & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
   return ATTN_OK;

@@ -1,0 +1,432 @@
+// bf16 attention backward, the dQ pass, on the sm_103a tensor cores
+// (tcgen05 + TMEM + TMA), d = 128.
+//
+// Recomputation backward of the "Flash Attention 2" post (ahmadsaeedzaidi.github.io
+// feed), section "Flash Attention 2", "Recomputation in backward pass": S and
+// P are rebuilt tile by tile from the saved row LSE, P = exp(scale·S - LSE).
+// With dP = dO Vᵀ and the row term D = rowsum(dO ∘ O) (preprocess kernel),
+// the Jacobian-vector product of the softmax-backward note
+// (shreyansh26.github.io feed), section "Backpropagating Through Softmax",
+// gives dS = P ∘ (dP - D), and dQ = scale·dS K.
+//
+// This pass owns one 128-row query tile (Q_i, dO_i resident in shared
+// memory) and streams the key/value tiles that the tile sees, so dQ_i is
+// accumulated in tensor memory and written once, in bf16: no float32
+// accumulator, no atomics, no conversion pass. dK and dV come from the
+// key-tile pass (bwd_tc.cu), which then needs no dQ work at all; the two
+// passes recompute S and dP each (two of the five GEMMs twice) in exchange
+// for full-width (N = 128) MMAs here and a short dependency chain there.
+//
+// GB300 mapping (rows = queries on the 128 TMEM lanes):
+//  * S_j = Q_i K_jᵀ into S0/S1 (two buffers), dP_j = dO_i V_jᵀ into dP,
+//    dQ += dS_j K_j into dQ (A = dS_j from tensor memory, bf16 pairs written
+//    over the consumed S_j columns).
+//  * Two softmax warpgroups split the 128 key columns of a step in halves;
+//    thread = query row, so LSE and D are per-thread scalars.
+//  * One converged MMA warp issues dP(j+1) as soon as dP(j) has been read,
+//    then dQ(j) and S(j+2) once the softmax of step j has written dS(j).
+//  * Every mbarrier wait is bounded (error word + abort flag + drain).
+
+#include "common.cuh"
+#include "launchers.h"
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace attn {
+
+ATTN_DEFINE_ERROR_WORD(take_error_bwd_dq)
+
+namespace {
+
+constexpr int kBM = 128;            // query rows per CTA (TMEM lanes)
+constexpr int kBN = 128;            // keys per step
+constexpr int kD = 128;             // head dimension of this pass
+constexpr int kThreads = 384;       // 12 warps
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DqCfg {
+  static constexpr int kTile = kBM * kD * 2;               // 32 KB bf16 tile (Q, dO, K_j, V_j)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kOffQ + kTile;
+  static constexpr int kOffK = kOffDO + kTile;             // [kKStages]
+  static constexpr int kOffV = kOffK + kKStages * kTile;   // [kVStages]
+  static constexpr int kSmemBytes = kOffV + kVStages * kTile;
+  static constexpr int kDynSmem = kSmemBytes + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
+  static_assert(kDynSmem + 256 <= 232448, "shared-memory budget");
+};
+
+struct DqBars {
+  uint64_t q_full;
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t dp_full, dp_free;
+  uint64_t dq_done, mma_drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+ATTN_DEVINL void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
+                              int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+ATTN_DEVINL void tma_store_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+ATTN_DEVINL void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+ATTN_DEVINL void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(ta), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+        "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Key tiles a 128-row query tile starting at row_first visits (0 if the tile
+// has no valid row); causal alignment is bottom-right.
+ATTN_DEVINL int key_tiles_for(int row_first, int Nq, int Nk, int causal) {
+  if (row_first >= Nq) return 0;
+  const int nk_tiles = (Nk + kBN - 1) / kBN;
+  if (!causal) return nk_tiles;
+  const int row_last = min(row_first + kBM - 1, Nq - 1);
+  return min(nk_tiles, (row_last + (Nk - Nq)) / kBN + 1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+              const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
+              const float* __restrict__ row_term, int Hq, int Hkv, int Nq, int Nk, float scale,
+              int causal, int n_qt) {
+  using C = DqCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ DqBars bars;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Head-major order, the heaviest (latest, for causal) query tile of each
+  // head first; a head's K/V stay in L2 while its query tiles run.
+  const int bh = int(blockIdx.x) / n_qt;
+  const int qt = n_qt - 1 - int(blockIdx.x) % n_qt;
+  const int b = bh / Hq, h = bh % Hq;
+  const int kvh = b * Hkv + h / (Hq / Hkv);
+  const int row0 = qt * kBM;
+  const int n = key_tiles_for(row0, Nq, Nk, causal);
+
+  if (tid == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.p_full[i], 256);     // both softmax warpgroups
+    }
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_free, 256);
+    mbar_init(&bars.dq_done, 1);
+    mbar_init(&bars.mma_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars.tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort;
+
+  // Register split, set inside each role: 128 x 80 (TMA, MMA, idle warps) +
+  // 256 x 208 (softmax) <= 384 x 168 registers the CTA is launched with.
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    regs_dec<80>();
+    if (lane == 0 && n > 0) {
+      tc::tma_prefetch_desc(&map_k);
+      tc::tma_prefetch_desc(&map_v);
+      mbar_arrive_expect_tx(&bars.q_full, 2 * C::kTile);
+      for (int a = 0; a < kD / 64; ++a) {
+        tc::tma_load_3d(smem + C::kOffQ + a * (kBM * 128), &map_q, 64 * a, row0, bh, &bars.q_full);
+        tc::tma_load_3d(smem + C::kOffDO + a * (kBM * 128), &map_do, 64 * a, row0, bh,
+                        &bars.q_full);
+      }
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const int sk = j % kKStages, sv = j % kVStages;
+        if (j >= kKStages) ok = mbar_wait_bounded(&bars.k_empty[sk], ((j / kKStages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars.k_full[sk], C::kTile);
+        for (int a = 0; a < kD / 64; ++a)
+          tc::tma_load_3d(smem + C::kOffK + sk * C::kTile + a * (kBN * 128), &map_k, 64 * a,
+                          j * kBN, kvh, &bars.k_full[sk]);
+        ++issued_k;
+        if (j >= kVStages) ok = mbar_wait_bounded(&bars.v_empty[sv], ((j / kVStages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars.v_full[sv], C::kTile);
+        for (int a = 0; a < kD / 64; ++a)
+          tc::tma_load_3d(smem + C::kOffV + sv * C::kTile + a * (kBN * 128), &map_v, 64 * a,
+                          j * kBN, kvh, &bars.v_full[sv]);
+        ++issued_v;
+      }
+      if (!ok) {
+        attn_flag_error(kErrTimeout);
+        bars.abort = 1;
+        // Drain: every load this thread issued has landed before the CTA exits.
+        mbar_wait_bounded(&bars.q_full, 0, nullptr);
+        for (int j = max(0, issued_k - kKStages); j < issued_k; ++j)
+          mbar_wait_bounded(&bars.k_full[j % kKStages], (j / kKStages) & 1, nullptr);
+        for (int j = max(0, issued_v - kVStages); j < issued_v; ++j)
+          mbar_wait_bounded(&bars.v_full[j % kVStages], (j / kVStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop; one elected lane issues each MMA.
+    regs_dec<80>();
+    if (n > 0) {
+      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false, false);   // S, dP
+      constexpr uint32_t idesc_q = tc::idesc_bf16_f32(kBM, kD, false, true);     // dQ
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      const uint32_t do_base = smem_u32(smem + C::kOffDO);
+      const uint32_t k_base = smem_u32(smem + C::kOffK);
+      const uint32_t v_base = smem_u32(smem + C::kOffV);
+      // X (128 x d, K-major) times Y_jᵀ (128 x d, K-major) into `col`
+      auto issue_qk = [&](uint32_t col, uint32_t xa, uint32_t ya) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
+          tc::mma_ss_warp(tmem + col, tc::smem_desc(xa + off, 16, 1024, tc::kLayoutSW128),
+                          tc::smem_desc(ya + off, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
+        }
+      };
+      auto s_col = [](int j) { return (j & 1) ? C::kColS1 : C::kColS0; };
+      auto issue_s = [&](int j) {
+        issue_qk(s_col(j), q_base, k_base + (j % kKStages) * C::kTile);
+        tc::mma_commit_warp(&bars.s_full[j & 1]);
+      };
+      auto issue_dp = [&](int j) {
+        issue_qk(C::kColDP, do_base, v_base + (j % kVStages) * C::kTile);
+        tc::mma_commit_warp(&bars.dp_full);
+        tc::mma_commit_warp(&bars.v_empty[j % kVStages]);   // V_j's only use
+      };
+      // dQ += dS_j K_j: A = dS_j pairs over the S_j columns (keys 64h..64h+63
+      // of warpgroup h at columns 64h .. 64h+31), B = K_j MN-major.
+      auto issue_dq = [&](int j) {
+        const uint32_t ka = k_base + (j % kKStages) * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t a_col = s_col(j) + (kk / 4) * 64 + (kk % 4) * 8;
+          tc::mma_ts_warp(tmem + C::kColDQ, tmem + a_col,
+                          tc::smem_desc(ka + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128), idesc_q,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit_warp(&bars.k_empty[j % kKStages]);   // K_j's last use
+      };
+
+      bool ok = mbar_wait_warp(&bars.q_full, 0, abort_flag);
+      if (ok) ok = mbar_wait_warp(&bars.k_full[0], 0, abort_flag);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_s(0);
+      }
+      if (ok) ok = mbar_wait_warp(&bars.v_full[0], 0, abort_flag);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_dp(0);
+      }
+      if (ok && n > 1) {
+        ok = mbar_wait_warp(&bars.k_full[1 % kKStages], 0, abort_flag);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_s(1);
+        }
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int j1 = j + 1, j2 = j + 2;
+        if (j1 < n) {
+          // dP(j+1) as soon as the softmax has read dP(j) and V_{j+1} is in
+          ok = mbar_wait2_warp(&bars.dp_free, j & 1, &bars.v_full[j1 % kVStages],
+                               (j1 / kVStages) & 1, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_dp(j1);
+        }
+        // K_{j+2} has normally landed long before: probe it with p_full(j)
+        const int ks = (j2 < n ? j2 : j) % kKStages;
+        const uint32_t kp = j2 < n ? (j2 / kKStages) & 1 : (j / kKStages) & 1;
+        ok = mbar_wait2_warp(&bars.p_full[j & 1], (j >> 1) & 1, &bars.k_full[ks], kp, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_dq(j);
+        if (j2 < n) issue_s(j2);   // over the S_j columns, after dQ(j) has read dS_j (issue order)
+      }
+      if (!ok && lane == 0) {
+        attn_flag_error(kErrTimeout);
+        bars.abort = 1;
+      }
+      __syncwarp();
+      tc::mma_commit_warp(&bars.dq_done);
+      // Drain: every MMA this warp issued has completed before TMEM is freed.
+      tc::mma_commit_warp(&bars.mma_drain);
+      mbar_wait_warp(&bars.mma_drain, 0, nullptr);
+    }
+  } else if (warp < 4) {
+    regs_dec<80>();                                // idle
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    regs_inc<208>();
+    const int half = (warp - 4) >> 2;              // key columns [64·half, 64·half + 64)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;             // query row in the tile (TMEM lane)
+    const int row = row0 + r;
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    const float c = scale * kLog2e;
+    const int shift = Nk - Nq;
+    const bool row_in = row < Nq;
+    const size_t ri = size_t(bh) * Nq + (row_in ? row : 0);
+    // rows past Nq: P = 0 (their dQ row is clipped by the store anyway)
+    const float nl = row_in ? -lse[ri] * kLog2e : -INFINITY;   // -LSE·log2e
+    const float nd = row_in ? -row_term[ri] : 0.f;             // -D
+    const int limit = causal ? min(Nk - 1, row + shift) : Nk - 1;   // last visible key
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait2_warp(&bars.s_full[j & 1], (j >> 1) & 1, &bars.dp_full, j & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t s_addr = tmem + lane_base + ((j & 1) ? C::kColS1 : C::kColS0) + half * 64;
+      uint32_t sr[64], dr[64];
+      tc::tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tc::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tc::tmem_ld32(tmem + lane_base + C::kColDP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tc::tmem_ld32(tmem + lane_base + C::kColDP + half * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tc::tmem_ld_wait();
+      tc::fence_before_sync();
+      mbar_arrive(&bars.dp_free);                  // dP(j+1) may overwrite dP now
+
+      // Keys past the end (zero-filled K rows) and, for causal, after the
+      // row's limit contribute nothing.
+      const int key0 = j * kBN + half * 64;
+      const bool masked = key0 + 63 > limit;
+      const f2 c2{c, c}, nl2{nl, nl}, nd2{nd, nd};
+      uint32_t pk[32];                             // dS_j as bf16 pairs
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const f2 x = fma2(f2{__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])}, c2, nl2);
+        f2 p{fast_exp2(x.x), fast_exp2(x.y)};
+        if (masked) {
+          if (key0 + 2 * e > limit) p.x = 0.f;
+          if (key0 + 2 * e + 1 > limit) p.y = 0.f;
+        }
+        const f2 dpd = add2(f2{__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])}, nd2);
+        const f2 ds = mul2(p, dpd);
+        pk[e] = pack_bf16x2(ds.x, ds.y);
+      }
+      // over the S_j columns this warpgroup has just read
+      tmem_st32(s_addr, pk);
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      mbar_arrive(&bars.p_full[j & 1]);
+    }
+
+    // Epilogue: dQ = scale·(Σ dS K) -> bf16 -> swizzled smem (the Q tile,
+    // read by no MMA any more) -> TMA store; warpgroup `half` owns the
+    // 64-dimension atom `half`.
+    if (ok && n > 0) ok = mbar_wait_bounded(&bars.dq_done, 0, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    uint8_t* atom = smem + C::kOffQ + half * (kBM * 128) + r * 128;
+    if (ok) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t v[32];
+        if (n > 0) {
+          tc::tmem_ld32(tmem + lane_base + C::kColDQ + half * 64 + ch * 32, v);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;  // no key is visible: dQ = 0
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * scale, __uint_as_float(v[2 * e + 1]) * scale);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = ch * 4 + u;
+          *reinterpret_cast<uint4*>(atom + ((chunk ^ (r & 7)) * 16)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+    } else {
+      if (lane == 0) attn_flag_error(kErrTimeout);
+      bars.abort = 1;
+    }
+    // Every warp of the warpgroup reaches this barrier, failed or not.
+    named_bar_sync(1 + half, kBM);
+    if (quarter == 0 && lane == 0 && !bars.abort && row0 < Nq) {
+      tma_store_3d(&map_dq, smem + C::kOffQ + half * (kBM * 128), 64 * half, row0, bh);
+      tma_store_commit_and_wait();
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const BwdArgs& a) {
+  using C = DqCfg;
+  if (a.d != kD) return cudaErrorInvalidValue;
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  const uint64_t bhq = uint64_t(a.B) * a.Hq, bhk = uint64_t(a.B) * a.Hkv;
+  if (!make_map_bf16_3d(&mq, a.q, kD, a.Nq, bhq, kBM) ||
+      !make_map_bf16_3d(&mdo, a.dO, kD, a.Nq, bhq, kBM) ||
+      !make_map_bf16_3d(&mk, a.k, kD, a.Nk, bhk, kBN) ||
+      !make_map_bf16_3d(&mv, a.v, kD, a.Nk, bhk, kBN) ||
+      !make_map_bf16_3d(&mdq, a.dq, kD, a.Nq, bhq, kBM))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kDynSmem);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (a.Nq + kBM - 1) / kBM;
+  const long blocks = long(n_qt) * a.B * a.Hq;
+  if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  bwd_dq_kernel<<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
+      mq, mk, mv, mdo, mdq, a.lse, a.row_term, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.causal, n_qt);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -17,19 +17,20 @@
 //  * Per step, with keys on the 128 TMEM lanes:
 //      Sᵀ = K_j Q_iᵀ and dPᵀ = V_j dO_iᵀ          (tcgen05.mma, fp32 in TMEM)
 //      Pᵀ = exp2(Sᵀ·scale·log2e - LSE·log2e), dSᵀ = Pᵀ ∘ (dPᵀ - D)
-//                                     (one warpgroup, one key row per thread,
-//                                      bf16 into swizzled shared memory)
-//      dV_j += Pᵀ dO_i, dK_j += dSᵀ Q_i           (TMEM accumulators, d columns)
-//      dQ_i  = dS K_j                             (TMEM; for d = 128 computed
-//                                      transposed, dQᵀ = K_jᵀ dSᵀ, so that
-//                                      M = 128)
-//    The next step's Sᵀ, dPᵀ are issued before this step's dV, dK, dQ so the
-//    softmax of step s+1 overlaps the tensor core's work of step s.
-//  * dQ has many writers (every key tile of the head); a third warpgroup
-//    drains each dQ tile from TMEM and adds it (scaled) into the float32
+//                                     (two warpgroups, one key row per thread;
+//                                      bf16 pairs back into TMEM)
+//      dV_j += Pᵀ dO_i, dK_j += dSᵀ Q_i           (A from TMEM, accumulators in
+//                                                  TMEM, d columns each)
+//  * d = 128: that is all this pass does; dQ comes from the query-tile pass
+//    (bwd_dq.cu). Two (Sᵀ, dPᵀ) buffers let one converged MMA warp issue
+//    dV(s), dK(s) and then Sᵀ/dPᵀ(s+2) back to back while the softmax works
+//    on step s+1: the tensor pipe runs the warp's MMAs in order, so step
+//    s+2 overwrites Pᵀ/dSᵀ(s) only after dV(s), dK(s) have read them.
+//  * d = 64 (BQ = 128, one buffer): dQ = dS K_j is computed here too, from a
+//    dSᵀ copy in shared memory, and a third warpgroup adds it into a float32
 //    accumulator with coalesced reductions; the attention-residuals lab
 //    (manishklach.github.io) reduces multi-writer gradients the same way.
-//    dK and dV have one writer: the CTA stores them once, by TMA.
+//  * dK and dV have one writer: the CTA stores them once, by TMA.
 //  * Every mbarrier wait is bounded (error word + abort flag + drain).
 
 #include "common.cuh"
@@ -50,34 +51,30 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D>
 struct BwdCfg {
   static constexpr int BQ = (D == 128) ? 64 : 128;        // query rows per step
-  static constexpr bool kDqTransposed = (D == 128);       // dQᵀ (M = d) vs dQ (M = BQ)
-  static constexpr int kPsBufs = (D == 128) ? 2 : 1;      // dSᵀ shared-memory buffers
-  static constexpr int kQStages = 3;                       // Q_i, dO_i, LSE, D ring
+  // d = 64: dQ = dS K_j (M = BQ) is computed here and added into the float32
+  // accumulator; d = 128: dQ comes from the query-tile pass.
+  static constexpr bool kFusedDq = (D == 64);
+  static constexpr int kPsBufs = kFusedDq ? 1 : 0;        // dSᵀ shared-memory buffers
+  static constexpr int kQStages = kFusedDq ? 3 : 4;       // Q_i, dO_i, LSE, D ring
   // shared memory (bytes; every tile 1024-aligned)
   static constexpr int kKVTile = kBK * D * 2;             // K_j or V_j
   static constexpr int kQTile = BQ * D * 2;               // Q_i or dO_i
-  static constexpr int kPsTile = kBK * BQ * 2;            // dSᵀ (bf16, the B operand of dQ)
+  static constexpr int kPsTile = kBK * BQ * 2;            // dSᵀ (bf16, the A operand of dQ)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kKVTile;
   static constexpr int kOffQ = kOffV + kKVTile;                      // [stage] Q, dO
   static constexpr int kOffP = kOffQ + kQStages * 2 * kQTile;       // [buf] dSᵀ
   static constexpr int kOffVec = kOffP + kPsBufs * kPsTile;         // [stage] -LSE·log2e, -D
-  // d = 128: dQ of one step staged row-major in float32 for the bulk
-  // reduction into the accumulator (128-byte aligned is enough unswizzled)
-  static constexpr int kOffDq = kOffVec + kQStages * 2 * BQ * 4;
-  static constexpr int kDqStageBytes = kDqTransposed ? BQ * D * 4 : 0;
-  static constexpr int kSmemBytes = kOffDq + kDqStageBytes;
+  static constexpr int kSmemBytes = kOffVec + kQStages * 2 * BQ * 4;
   static constexpr int kDynSmem = kSmemBytes + 1024;
   // tensor memory columns. d = 128: two (Sᵀ, dPᵀ) buffers of 64 + 64
-  // columns; dQᵀ(s) is written over the Sᵀ columns of its own buffer once the
-  // softmax has read them; dV, dK 128 each (2·128 + 2·128 = 512). d = 64:
-  // one (Sᵀ, dPᵀ) buffer of 128 + 128, two dQ buffers of 64, dV, dK 64 each.
-  static constexpr int kSdpBufs = (D == 128) ? 2 : 1;
-  static constexpr bool kDqInS = (D == 128);
+  // columns, dV, dK 128 each (2·128 + 2·128 = 512). d = 64: one (Sᵀ, dPᵀ)
+  // buffer of 128 + 128, two dQ buffers of 64, dV, dK 64 each.
+  static constexpr int kSdpBufs = kFusedDq ? 1 : 2;
   static constexpr uint32_t kSdpCols = 2 * BQ;
   static constexpr uint32_t kColDQ = kSdpBufs * kSdpCols;            // d = 64 only
-  static constexpr uint32_t kDqCols = kDqTransposed ? BQ : D;
-  static constexpr uint32_t kColDV = kDqInS ? kSdpBufs * kSdpCols : kColDQ + 2 * kDqCols;
+  static constexpr uint32_t kDqCols = D;
+  static constexpr uint32_t kColDV = kFusedDq ? kColDQ + 2 * kDqCols : kSdpBufs * kSdpCols;
   static constexpr uint32_t kColDK = kColDV + D;
   static_assert(kColDK + D <= 512, "TMEM budget");
   __host__ __device__ static constexpr uint32_t col_s(int b) { return b * kSdpCols; }
@@ -89,17 +86,16 @@ struct BwdCfg {
   __host__ __device__ static constexpr uint32_t col_pair(int q0) {
     return (q0 / CW) * CW + (q0 % CW) / 2;
   }
-  static_assert(kOffDq % 128 == 0, "bulk-copy source alignment");
   static_assert(kDynSmem + 256 <= 232448, "shared-memory budget (dynamic + static)");
 };
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t q_full[3], q_empty[3];
+  uint64_t q_full[4], q_empty[4];
   uint64_t sdp_full[2], p_full[2];
   uint64_t ps_free[2];
   uint64_t dq_full[2], dq_free[2];
-  uint64_t dkv_full, mma_drain, mma_drain2;
+  uint64_t dkv_full, mma_drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -117,30 +113,6 @@ ATTN_DEVINL void tma_store_commit_and_wait() {
 }
 ATTN_DEVINL void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Bulk tensor reduction: add the shared-memory box at `smem_src` into the
-// float32 tensor of `map` at coordinates (c0, c1, c2).
-ATTN_DEVINL void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
-                                   int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];"
-      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-ATTN_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-ATTN_DEVINL void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-ATTN_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Named barrier over `count` threads that also ANDs `pred` across them.
-ATTN_DEVINL bool named_bar_and(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r) : "r"(uint32_t(pred)), "r"(id), "r"(count) : "memory");
-  return r != 0;
 }
 ATTN_DEVINL void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
@@ -204,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
-              const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse, const float* __restrict__ row_term,
+              const float* __restrict__ lse, const float* __restrict__ row_term,
               float* __restrict__ dq_acc, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
               int n_ktiles) {
   using C = BwdCfg<D>;
@@ -248,7 +220,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     mbar_init(&bars.p_full[1], 256);
     mbar_init(&bars.dkv_full, 1);
     mbar_init(&bars.mma_drain, 1);
-    mbar_init(&bars.mma_drain2, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -350,16 +321,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     regs_dec<120>();
     {
       constexpr uint32_t idesc_kv = tc::idesc_bf16_f32(kBK, D, false, true);
-      constexpr uint32_t idesc_dq = C::kDqTransposed ? tc::idesc_bf16_f32(D, BQ, true, true)
-                                                     : tc::idesc_bf16_f32(BQ, D, true, true);
+      constexpr uint32_t idesc_dq = tc::idesc_bf16_f32(BQ, D, true, true);    // d = 64 only
       // Base descriptors; a descriptor's start-address field is (bytes >> 4),
       // so moving inside a tile adds (offset >> 4) to the 64-bit value.
       const uint64_t k_mn = tc::smem_desc(smem_u32(smem + C::kOffK), kBK * 128, 1024, tc::kLayoutSW128);
-      auto q_km = [&](int st, int which) {   // Q (0) or dO (1) of a stage, K-major
-        return tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2 + which) * C::kQTile), 16, 1024,
-                             tc::kLayoutSW128);
-      };
-      auto q_mn = [&](int st, int which) {   // the same tile as an MN-major operand
+      auto q_mn = [&](int st, int which) {   // Q (0) or dO (1) of a stage, MN-major
         return tc::smem_desc(smem_u32(smem + C::kOffQ + (st * 2 + which) * C::kQTile), BQ * 128,
                              1024, tc::kLayoutSW128);
       };
@@ -369,12 +335,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       };
       auto issue_sdp = [&](int s) { bwd_issue_sdp<D>(smem, tmem, s, &bars.sdp_full[s % C::kSdpBufs]); };
 
-      // dV += Pᵀ dO ; dK += dSᵀ Q ; dQ(ᵀ)   for step s (after its p_full)
+      // dV += Pᵀ dO ; dK += dSᵀ Q (; d = 64: dQ = dS K_j)   for step s (after its p_full)
       auto issue_grads = [&](int s) {
         const int st = s % C::kQStages;
-        const int pb = s % C::kPsBufs;
         const int b = s % C::kSdpBufs;
-        const int db = s & 1;
         {
           // A = Pᵀ / dSᵀ from tensor memory (bf16 pairs), B = dO / Q MN-major
           const uint64_t dob = q_mn(st, 1), qb = q_mn(st, 0);
@@ -388,67 +352,49 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           }
         }
         tc::mma_commit_warp(&bars.q_empty[st]);      // Q_i, dO_i, LSE, D of the stage consumed
-        {
-          // dQᵀ = K_jᵀ dSᵀ (A = K_j MN-major over d atoms, B = dSᵀ) for d = 128;
-          // dQ = dS K_j (A = dSᵀ MN-major over query atoms, B = K_j) for d = 64.
-          const uint32_t dq_col = C::kDqInS ? C::col_s(b) : C::kColDQ + db * C::kDqCols;
-          const uint64_t s_mn = ps_mn(pb);
-          const uint64_t a0 = C::kDqTransposed ? k_mn : s_mn;
-          const uint64_t b0 = C::kDqTransposed ? s_mn : k_mn;
+        if (C::kFusedDq) {
+          // dQ = dS K_j (A = dSᵀ MN-major over query atoms, B = K_j) into dQ buffer s & 1
+          const int db = s & 1;
+          const uint64_t a0 = ps_mn(0), b0 = k_mn;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t step = uint64_t(kk * 2048) >> 4;   // 16 keys down both operands
-            tc::mma_ss_warp(tmem + dq_col, a0 + step, b0 + step, idesc_dq, kk > 0);
+            tc::mma_ss_warp(tmem + C::kColDQ + db * C::kDqCols, a0 + step, b0 + step, idesc_dq,
+                            kk > 0);
           }
+          tc::mma_commit_warp(&bars.dq_full[db]);
+          tc::mma_commit_warp(&bars.ps_free[0]);
         }
-        tc::mma_commit_warp(&bars.dq_full[db]);
-        tc::mma_commit_warp(&bars.ps_free[pb]);
       };
 
+      // Issue order: Sᵀ/dPᵀ of the first kSdpBufs steps, then per step s the
+      // gradients of s followed by Sᵀ/dPᵀ(s + kSdpBufs) into the buffer step s
+      // used. The tensor pipe runs this warp's MMAs in order, so the new
+      // scores overwrite Pᵀ/dSᵀ(s) only after the gradients of s have read them.
       bool ok = true;
       if (n > 0) ok = mbar_wait_warp(&bars.kv_full, 0, abort_flag);
-      if (C::kSdpBufs == 1 && n > 0 && ok) {   // the single buffer's first fill
-        ok = mbar_wait_warp(&bars.q_full[0], 0, abort_flag);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_sdp(0);
-        }
+      for (int t = 0; t < min(n, C::kSdpBufs) && ok; ++t) {
+        ok = mbar_wait_warp(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_sdp(t);
       }
-      if (C::kSdpBufs == 1) {
-        // One (Sᵀ, dPᵀ) buffer, which also holds Pᵀ, dSᵀ of the step: the
-        // gradients of step s are issued first, then the buffer is refilled
-        // with step s+1 (the tensor pipe executes in issue order).
-        for (int s = 0; s < n && ok; ++s) {
-          ok = mbar_wait_warp(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
+      for (int s = 0; s < n && ok; ++s) {
+        // Q/dO of step s + kSdpBufs have normally landed long before: probe
+        // them together with p_full(s)
+        const int tq = s + C::kSdpBufs < n ? s + C::kSdpBufs : s;
+        ok = mbar_wait2_warp(&bars.p_full[s & 1], (s >> 1) & 1, &bars.q_full[tq % C::kQStages],
+                             (tq / C::kQStages) & 1, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        if (C::kFusedDq && s >= 2) {   // dQ TMEM buffer s & 1 drained (step s-2)
+          ok = mbar_wait_warp(&bars.dq_free[s & 1], ((s >> 1) - 1) & 1, abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
-          if (s >= 2) {   // dQ TMEM buffer s & 1 drained (step s-2)
-            ok = mbar_wait_warp(&bars.dq_free[s & 1], ((s >> 1) - 1) & 1, abort_flag);
-            if (!ok) break;
-            tc::fence_after_sync();
-          }
-          issue_grads(s);
-          if (s + 1 < n) {
-            const int s1 = s + 1;
-            ok = mbar_wait_warp(&bars.q_full[s1 % C::kQStages], (s1 / C::kQStages) & 1,
-                                abort_flag);
-            if (!ok) break;
-            tc::fence_after_sync();
-            issue_sdp(s1);
-          }
         }
-      } else {
-        // Two buffers: this thread issues the gradient MMAs of every step
-        // (after its softmax); warp 3 issues Sᵀ/dPᵀ (see below). tcgen05.mma
-        // issue returns only as the tensor pipe accepts the instruction, so
-        // one thread serving both streams would sit on one barrier while the
-        // other stream's work is ready.
-        for (int s = 0; s < n && ok; ++s) {
-          ok = mbar_wait_warp(&bars.p_full[s & 1], (s >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_grads(s);
-        }
+        issue_grads(s);
+        const int t = s + C::kSdpBufs;
+        if (t < n) issue_sdp(t);
       }
       if (!ok && lane == 0) {
         attn_flag_error(kErrTimeout);
@@ -460,28 +406,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       mbar_wait_warp(&bars.mma_drain, 0, nullptr);
     }
   } else if (warp == 3) {
-    // ---------------------------------------------------------- Sᵀ/dPᵀ issuer (d = 128)
-    // The whole warp runs this loop; one elected lane issues each MMA.
-    regs_dec<120>();
-    if (C::kSdpBufs == 2 && n > 0) {
-      bool ok = mbar_wait_warp(&bars.kv_full, 0, abort_flag);
-      for (int t = 0; t < n && ok; ++t) {
-        // buffer t & 1 must be drained of dQᵀ(t-2); Q/dO(t) loaded
-        if (t >= 2) ok = mbar_wait_warp(&bars.dq_free[t & 1], ((t - 2) >> 1) & 1, abort_flag);
-        if (ok) ok = mbar_wait_warp(&bars.q_full[t % C::kQStages], (t / C::kQStages) & 1,
-                                    abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        bwd_issue_sdp<D>(smem, tmem, t, &bars.sdp_full[t & 1]);
-      }
-      if (!ok && lane == 0) {
-        attn_flag_error(kErrTimeout);
-        bars.abort = 1;
-      }
-      __syncwarp();
-      tc::mma_commit_warp(&bars.mma_drain2);
-      mbar_wait_warp(&bars.mma_drain2, 0, nullptr);
-    }
+    regs_dec<120>();                                 // idle
   } else if (warp >= 4 && warp < 12) {
     // ---------------------------------------------------------- Pᵀ, dSᵀ warpgroups
     // Two warpgroups share the key rows (TMEM lanes) and split the BQ query
@@ -499,19 +424,18 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     bool ok = true;
     for (int s = 0; s < n; ++s) {
       const int st = s % C::kQStages;
-      const int pb = s % C::kPsBufs;
       int hh, qt;
       plan.at(s, hh, qt);
       const int q0 = qt * BQ;
       const int b = s % C::kSdpBufs;
-      bool w = mbar_wait_bounded(&bars.sdp_full[b], (s / C::kSdpBufs) & 1, abort_flag);
-      w = w && mbar_wait_bounded(&bars.q_full[st], (s / C::kQStages) & 1, abort_flag);
-      if (s >= C::kPsBufs)
-        w = w && mbar_wait_bounded(&bars.ps_free[pb], ((s / C::kPsBufs) - 1) & 1, abort_flag);
+      bool w = mbar_wait2_warp(&bars.sdp_full[b], (s / C::kSdpBufs) & 1, &bars.q_full[st],
+                               (s / C::kQStages) & 1, abort_flag);
+      if (C::kFusedDq && s >= 1)   // the dSᵀ copy of step s-1 has been read by dQ(s-1)
+        w = w && mbar_wait_bounded(&bars.ps_free[0], (s - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc::fence_after_sync();
       const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * BQ * 4);
-      uint8_t* dst = smem + C::kOffP + pb * C::kPsTile;
+      uint8_t* dst = smem + C::kOffP;
       const bool key_in = key < Nk;
       // first visible query column of this key row (causal), relative to q0
       const int qmin = causal ? key - shift - q0 : -1;
@@ -551,7 +475,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             }
           }
           const uint32_t off = sw128_offset(r, col0 + g8 * 8, kBK);
-          *reinterpret_cast<uint4*>(dst + off) =
+          if (C::kFusedDq)             // dSᵀ copy for dQ = dS K_j
+            *reinterpret_cast<uint4*>(dst + off) =
               make_uint4(dk[4 * g8], dk[4 * g8 + 1], dk[4 * g8 + 2], dk[4 * g8 + 3]);
         }
         // Pᵀ and dSᵀ pairs over the columns just read (A operands of dV, dK)
@@ -573,63 +498,39 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                 // TMEM lane
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    // d = 128: the dQᵀ tile (lane = dimension) is scaled, written row-major
-    // into the float32 staging buffer and added into the accumulator with one
-    // bulk tensor reduction per step (the tensor memory is released right
-    // after the load). d = 64: lane = query row, 16-byte reductions per row.
-    const bool bulk_issuer = quarter == 0 && lane == 0;
-    float* stage = reinterpret_cast<float*>(smem + C::kOffDq);
+    // d = 64: lane = query row, 64 columns = the dimensions; 16-byte
+    // reductions into the float32 accumulator. d = 128 has no dQ here.
     bool ok = true;
-    for (int s = 0; s < n; ++s) {
+    for (int s = 0; s < (C::kFusedDq ? n : 0); ++s) {
       const int db = s & 1;
       int hh, qt;
       plan.at(s, hh, qt);
       const size_t bh = size_t(b) * Hq + g * group + hh;
       const int q0 = qt * BQ;
-      const bool got = mbar_wait_bounded(&bars.dq_full[db], (s >> 1) & 1, abort_flag);
-      // The whole warpgroup agrees on the outcome (its barriers below need all
-      // 128 threads); for d = 128 this barrier also tells every thread that the
-      // bulk reduction of step s-1 has finished reading the staging buffer.
-      ok = C::kDqTransposed ? named_bar_and(1, 128, got) : __all_sync(0xffffffffu, got);
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars.dq_full[db], (s >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
       tc::fence_after_sync();
-      const uint32_t col0 = C::kDqInS ? C::col_s(s % C::kSdpBufs) : C::kColDQ + db * C::kDqCols;
+      const uint32_t col0 = C::kColDQ + db * C::kDqCols;
       uint32_t v0[32], v1[32];
       tc::tmem_ld32(tmem + lane_base + col0, v0);
       tc::tmem_ld32(tmem + lane_base + col0 + 32, v1);
       tc::tmem_ld_wait();
       tc::fence_before_sync();
       mbar_arrive(&bars.dq_free[db]);
-      if (C::kDqTransposed) {
-        // stage[q][d]: for each query a warp writes 32 consecutive floats
+      if (q0 + r < Nq) {
+        float* row = dq_acc + (bh * Nq + q0 + r) * D;
 #pragma unroll
-        for (int e = 0; e < BQ; ++e)
-          stage[e * D + r] = __uint_as_float(e < 32 ? v0[e] : v1[e - 32]) * scale;
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (bulk_issuer) {
-          // rows past Nq fall outside the map and are not written
-          tma_reduce_add_3d(&map_dq, stage, 0, q0, int(bh));
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-      } else {
-        // lane r = query row, columns = the d (= 64) dimensions
-        if (q0 + r < Nq) {
-          float* row = dq_acc + (bh * Nq + q0 + r) * D;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            red_add_v4(row + e, __uint_as_float(v0[e]) * scale, __uint_as_float(v0[e + 1]) * scale,
-                       __uint_as_float(v0[e + 2]) * scale, __uint_as_float(v0[e + 3]) * scale);
-            red_add_v4(row + 32 + e, __uint_as_float(v1[e]) * scale,
-                       __uint_as_float(v1[e + 1]) * scale, __uint_as_float(v1[e + 2]) * scale,
-                       __uint_as_float(v1[e + 3]) * scale);
-          }
+        for (int e = 0; e < 32; e += 4) {
+          red_add_v4(row + e, __uint_as_float(v0[e]) * scale, __uint_as_float(v0[e + 1]) * scale,
+                     __uint_as_float(v0[e + 2]) * scale, __uint_as_float(v0[e + 3]) * scale);
+          red_add_v4(row + 32 + e, __uint_as_float(v1[e]) * scale,
+                     __uint_as_float(v1[e + 1]) * scale, __uint_as_float(v1[e + 2]) * scale,
+                     __uint_as_float(v1[e + 3]) * scale);
         }
       }
     }
-    // every bulk reduction of this CTA has landed before it exits
-    if (C::kDqTransposed && bulk_issuer) bulk_wait_all();
     // dK = scale·(dSᵀ Q summed), dV = Pᵀ dO summed -> bf16 -> K_j / V_j tiles -> TMA store.
     if (ok && n > 0)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.dkv_full, 0, abort_flag));
@@ -691,7 +592,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 template <int D>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
-  CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   const uint64_t bhq = uint64_t(a.B) * a.Hq, bhk = uint64_t(a.B) * a.Hkv;
   if (!make_map_bf16_3d(&mq, a.q, D, a.Nq, bhq, C::BQ) ||
       !make_map_bf16_3d(&mdo, a.dO, D, a.Nq, bhq, C::BQ) ||
@@ -700,11 +601,6 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
       !make_map_bf16_3d(&mdk, a.dk, D, a.Nk, bhk, kBK) ||
       !make_map_bf16_3d(&mdv, a.dv, D, a.Nk, bhk, kBK))
     return cudaErrorInvalidValue;
-  if (C::kDqTransposed) {
-    if (!make_map_f32_3d(&mdq, a.dq_acc, D, a.Nq, bhq, D, C::BQ)) return cudaErrorInvalidValue;
-  } else {
-    mdq = mq;   // unused: d = 64 adds dQ with per-row reductions
-  }
   cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
@@ -712,7 +608,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   const long blocks = long(n_ktiles) * a.B * a.Hkv;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
   bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
-      mq, mk, mv, mdo, mdk, mdv, mdq, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale,
+      mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale,
       a.causal, n_ktiles);
   return cudaGetLastError();
 }

@@ -40,6 +40,7 @@ struct BwdArgs {
   float* row_term;   // D = rowsum(dO ∘ O), [B, Hq, Nq]
   float* dq_acc;     // float32 dQ accumulator, [B, Hq, Nq, d]
   cudaStream_t stream;
+  bool zero_dq_acc;  // the preprocess zeroes dq_acc (the passes that add into it)
 };
 
 struct DecodeArgs {
@@ -76,6 +77,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a);
 cudaError_t launch_bwd_simt(const BwdArgs& a);
 cudaError_t launch_bwd_tc(const BwdArgs& a);
+cudaError_t launch_bwd_dq(const BwdArgs& a);
 cudaError_t launch_bwd_convert(const BwdArgs& a);
 cudaError_t launch_decode_split(const DecodeArgs& a);
 cudaError_t launch_merge(const MergeArgs& a);
@@ -83,6 +85,7 @@ cudaError_t launch_merge(const MergeArgs& a);
 // Per-translation-unit device error words (read and cleared).
 uint32_t take_error_fwd_tc();
 uint32_t take_error_bwd_tc();
+uint32_t take_error_bwd_dq();
 uint32_t take_error_decode();
 
 }  // namespace attn
