@@ -24,6 +24,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
 bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO,
                       float* __restrict__ row_term, float* __restrict__ dq_acc, long rows) {
+  // the key-tile pass (d = 128) may launch while this grid's last blocks run;
+  // it waits for this grid before reading the row term
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   if constexpr (sizeof(T) == 2) {
     constexpr int kLanesPerRow = D / 8;

@@ -424,9 +424,23 @@ cudaError_t launch_bwd_dq(const BwdArgs& a) {
   const int n_qt = (a.Nq + kBM - 1) / kBM;
   const long blocks = long(n_qt) * a.B * a.Hq;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-  bwd_dq_kernel<<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
-      mq, mk, mv, mdo, mdq, a.lse, a.row_term, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.causal, n_qt);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the key-tile pass: it reads only
+  // the inputs and the preprocess's row term (complete before that pass
+  // started), so it needs no grid-dependency wait and fills the SMs that the
+  // key-tile pass's last wave leaves idle.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_dq_kernel, mq, mk, mv, mdo, mdq, a.lse,
+                            static_cast<const float*>(a.row_term), a.Hq, a.Hkv, a.Nq, a.Nk,
+                            a.scale, a.causal, n_qt);
 }
 
 }  // namespace attn

@@ -181,6 +181,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               int n_ktiles) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
+  // The dQ pass that follows (d = 128) reads none of this kernel's outputs:
+  // let it start on the SMs this grid's last wave leaves idle.
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -282,6 +285,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     // free up, so their latency overlaps the wait.
     constexpr int kPer = BQ / 32;
     float nl[kPer], nd[kPer];
+    // d = 128 launches as a programmatic dependent of the preprocess: the row
+    // term D is read only once that grid has completed (a no-op otherwise).
+    pdl_wait_primary();
     auto fetch = [&](int s) {
       int hh, qt;
       plan.at(s, hh, qt);
@@ -607,10 +613,29 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   const int n_ktiles = (a.Nk + kBK - 1) / kBK;
   const long blocks = long(n_ktiles) * a.B * a.Hkv;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-  bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
-      mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale,
-      a.causal, n_ktiles);
-  return cudaGetLastError();
+  if (C::kFusedDq) {
+    // d = 64 adds into the accumulator the preprocess zeroes: plain launch
+    bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
+        mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk,
+        a.scale, a.causal, n_ktiles);
+    return cudaGetLastError();
+  }
+  // d = 128: programmatic dependent of the preprocess; only the LSE/D loader
+  // waits for it (it reads the row term), the prologue (TMEM, K/V, Q/dO
+  // loads) overlaps the preprocess's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D>, mq, mk, mv, mdo, mdk, mdv, a.lse,
+                            static_cast<const float*>(a.row_term), a.dq_acc, a.Hq, a.Hkv, a.Nq,
+                            a.Nk, a.scale, a.causal, n_ktiles);
 }
 
 }  // namespace

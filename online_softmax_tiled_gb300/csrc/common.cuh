@@ -97,6 +97,16 @@ ATTN_DEVINL float max3(float a, float b, float c) {
   return d;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start once every CTA of the preceding kernel has executed
+// launch_dependents (or exited); wait_primary blocks until that kernel has
+// completed and its memory is visible. A kernel that does not read what the
+// preceding kernel writes need not wait.
+ATTN_DEVINL void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+ATTN_DEVINL void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Register re-split between warpgroups (all warps of a warpgroup execute it).
 template <int N> ATTN_DEVINL void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));

@@ -56,6 +56,8 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
   constexpr int kRowBytes = D * 2;
   constexpr int kStageBytes = kStageKeys * kRowBytes;
+  // the merge kernel may launch (and wait for this grid) as the last wave runs
+  pdl_launch_dependents();
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sK = smem;
   uint8_t* sV = smem + kStages * kStageBytes;
@@ -285,6 +287,9 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
              const float* __restrict__ l_part, TOut* __restrict__ o, float* __restrict__ lse,
              int rows, int S, int d) {
   constexpr int kBatch = 8;
+  // Launched as a programmatic dependent: the partials are read only after
+  // the preceding (split) grid has completed.
+  pdl_wait_primary();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -369,16 +374,23 @@ cudaError_t launch_decode_split(const DecodeArgs& a) {
 }
 
 cudaError_t launch_merge(const MergeArgs& a) {
-  const unsigned blocks = unsigned((a.rows + 7) / 8);
+  // Programmatic dependent launch: the merge's launch overlaps the tail of
+  // the kernel before it; the kernel waits for that grid before reading.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((a.rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (a.out_dt == ATTN_F32)
-    merge_kernel<float><<<blocks, 256, 0, a.stream>>>(a.o_part, a.m_part, a.l_part,
-                                                      static_cast<float*>(a.o), a.lse, a.rows,
-                                                      a.num_splits, a.d);
-  else
-    merge_kernel<__nv_bfloat16><<<blocks, 256, 0, a.stream>>>(
-        a.o_part, a.m_part, a.l_part, static_cast<__nv_bfloat16*>(a.o), a.lse, a.rows,
-        a.num_splits, a.d);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, merge_kernel<float>, a.o_part, a.m_part, a.l_part,
+                              static_cast<float*>(a.o), a.lse, a.rows, a.num_splits, a.d);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, a.o_part, a.m_part, a.l_part,
+                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.rows, a.num_splits, a.d);
 }
 
 }  // namespace attn
