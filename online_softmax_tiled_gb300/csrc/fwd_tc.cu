@@ -126,6 +126,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   // tile). d = 128 (P̃ over the scores): one thread in the interleaved order
   // S0, S1, PV0, S0', PV1, S1', ... measured faster there.
   constexpr int kIssuers = C::kSeparateP ? 2 : 1;
+  // Launched as a programmatic dependent of whatever precedes it in the
+  // stream: the prologue (barriers, TMEM) overlaps that kernel's tail and
+  // the TMA producer waits for it before the first load. Every global access
+  // of this kernel follows those loads.
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -179,6 +184,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     regs_dec<80>();
+    pdl_wait_primary();
     if (lane == 0 && nj > 0) {
       tc::tma_prefetch_desc(&map_q);
       tc::tma_prefetch_desc(&map_k);
@@ -584,9 +590,18 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
   const int n_qblk = (a.Nq + 2 * kBM - 1) / (2 * kBM);
   const long blocks = long(n_qblk) * a.B * a.Hq;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
-  fwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
-      mq, mk, mv, mo, a.lse, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.causal, n_qblk);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D>, mq, mk, mv, mo, a.lse, a.Hq, a.Hkv, a.Nq,
+                            a.Nk, a.scale, a.causal, n_qblk);
 }
 
 }  // namespace
