@@ -82,6 +82,10 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
     fence_barrier_init();
   }
+  // Launched as a programmatic dependent: every global access of this grid
+  // (q, the KV cache, the partials a previous merge may still be reading)
+  // comes after the preceding grid has completed.
+  pdl_wait_primary();
   __syncthreads();
 
   auto issue = [&](int st) {
@@ -288,8 +292,10 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
              int rows, int S, int d) {
   constexpr int kBatch = 8;
   // Launched as a programmatic dependent: the partials are read only after
-  // the preceding (split) grid has completed.
+  // the preceding (split) grid has completed. Whatever follows may launch
+  // early and wait for this grid the same way.
   pdl_wait_primary();
+  pdl_launch_dependents();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -348,12 +354,21 @@ cudaError_t launch_split_t(const DecodeArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_splits, a.Hkv, a.B);
-  decode_split_kernel<D, G><<<grid, kThreads, smem, a.stream>>>(
-      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
-      static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part, a.Hq, a.Hkv, a.L,
-      a.num_splits, a.scale);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_splits, a.Hkv, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G>,
+                            static_cast<const __nv_bfloat16*>(a.q),
+                            static_cast<const __nv_bfloat16*>(a.k),
+                            static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part,
+                            a.Hq, a.Hkv, a.L, a.num_splits, a.scale);
 }
 
 template <int D>
