@@ -40,6 +40,12 @@ SMALL = [
     (1, 1, 1, 1, 77, 64, "bf16", False),
     (1, 2, 2, 100, 100, 64, "f32", True),
     (1, 4, 1, 90, 150, 128, "f32", False),
+    # d = 128 bf16 runs the key-tile and query-tile passes: ragged tails on
+    # both sides, Nq < Nk and Nq > Nk, one query row, GQA 8:1
+    (1, 2, 2, 130, 390, 128, "bf16", True),
+    (1, 8, 1, 200, 333, 128, "bf16", False),
+    (1, 1, 1, 1, 300, 128, "bf16", True),
+    (1, 2, 2, 513, 129, 128, "bf16", False),
 ]
 
 
