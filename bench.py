@@ -247,6 +247,8 @@ def kernel_label(w):
         return ("fwd_simt_kernel" if w.dtype == "f32" else "fwd_tc_kernel") + \
             " (whole attn_fwd call, one launch)"
     if w.kind == "bwd":
+        if w.dtype == "bf16" and w.d == 128:
+            return "attn_bwd call (row-term preprocess + dK/dV key-tile pass + dQ query-tile pass)"
         return "attn_bwd call (row-term preprocess + main kernel + dQ convert)"
     return "attn_decode_splitkv call (split kernel + merge kernel)"
 
