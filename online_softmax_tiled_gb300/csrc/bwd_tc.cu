@@ -490,7 +490,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         tc::tmem_st16(tmem + lane_base + C::col_dp(b) + C::col_pair(col0), dk);
       }
       tc::tmem_st_wait();
-      fence_proxy_async_smem();      // generic-proxy writes -> tensor-core (async proxy) reads
+      // generic-proxy writes of the dSᵀ copy -> tensor-core (async proxy) reads
+      if (C::kFusedDq) fence_proxy_async_smem();
       tc::fence_before_sync();
       mbar_arrive(&bars.p_full[s & 1]);
     }
