@@ -28,6 +28,8 @@ from .attention import (  # noqa: F401
     tiled_forward,
     decode_split_partials,
     merge_partials,
+    gather_paged,
+    decode_paged,
     decode_splitkv,
     default_scale,
 )

@@ -23,6 +23,9 @@ Sources, by page and section:
   maximum, independent of chunk order.
 * Attention-residuals kernel lab (manishklach.github.io), §Phase 2: a
   partition with no entries contributes exactly zero mass to the merge.
+* ML notes, prefill/decode and the KV cache: a serving cache is kept in
+  fixed-size blocks reached through a per-request block table
+  (``gather_paged``, ``decode_paged``).
 
 Readings where the pages are silent (each also listed in the design notes):
 
@@ -327,6 +330,48 @@ def decode_splitkv(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     """Decode output through the split-and-merge route: O [B, Hq, d],
     LSE [B, Hq]."""
     return merge_partials(*decode_split_partials(q, k, v, scale, num_splits))
+
+
+def gather_paged(pages: np.ndarray, table_row: np.ndarray, length: int,
+                 page_size: int) -> np.ndarray:
+    """The logical cache [Hkv, length, d] of one request from a paged pool.
+
+    ML notes (prefill/decode and the KV cache): the cache lives in
+    fixed-size blocks and a per-request block table maps logical block
+    t // page_size to a physical page; token t is row t % page_size of that
+    page. pages: [num_pages, Hkv, page_size, d]; table_row: [max_pages].
+    """
+    t = np.arange(length)
+    phys = table_row[t // page_size]
+    return pages[phys, :, t % page_size, :].transpose(1, 0, 2)
+
+
+def decode_paged(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
+                 block_table: np.ndarray, seq_lens: np.ndarray, page_size: int,
+                 scale: float):
+    """Query-length-1 attention of every request over its own tokens, read
+    through its block table: O [B, Hq, d], LSE [B, Hq].
+
+    Per request b and query head h (contiguous GQA grouping), over the
+    request's seq_lens[b] tokens: S = scale · K q, P = softmax(S), O = P V,
+    LSE = ln Σ exp(S). A request with no token has O = 0, LSE = -inf.
+    """
+    B, Hq, _ = q.shape
+    Hkv = k_pages.shape[1]
+    o = np.zeros((B, Hq, v_pages.shape[-1]))
+    lse = np.full((B, Hq), NEG_INF)
+    for b in range(B):
+        length = int(seq_lens[b])
+        if length == 0:
+            continue
+        k = gather_paged(k_pages, block_table[b], length, page_size)
+        v = gather_paged(v_pages, block_table[b], length, page_size)
+        for h in range(Hq):
+            g = _kv_head(h, Hq, Hkv)
+            sc = scale * (k[g] @ q[b, h])
+            o[b, h] = softmax_rows(sc[None, :])[0] @ v[g]
+            lse[b, h] = logsumexp_rows(sc[None, :])[0]
+    return o, lse
 
 
 def default_scale(d: int) -> float:

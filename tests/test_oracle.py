@@ -436,3 +436,78 @@ def test_planted_mistakes_are_caught(monkeypatch):
                 except Exception:  # a crash also counts as caught
                     errs.append(np.inf)
             assert max(errs) > 1e-6, f"pins missed the planted mistake: {name}"
+
+
+# --------------------------------------------------------------------------
+# Paged, variable-length decode
+# --------------------------------------------------------------------------
+
+def _paged_from_contiguous(k, page_size, rng):
+    """Cut a contiguous cache [B, Hkv, L, d] into pages [P, Hkv, page_size, d]
+    placed at random physical indices; returns (pages, block_table)."""
+    B, Hkv, L, d = k.shape
+    per = -(-L // page_size)
+    perm = rng.permutation(B * per)
+    pages = np.zeros((B * per, Hkv, page_size, d))
+    table = np.zeros((B, per), dtype=np.int64)
+    for b in range(B):
+        for i in range(per):
+            lo, hi = i * page_size, min((i + 1) * page_size, L)
+            phys = perm[b * per + i]
+            pages[phys, :, : hi - lo] = k[b, :, lo:hi]
+            table[b, i] = phys
+    return pages, table
+
+
+def test_paged_decode_equals_attention_on_the_gathered_cache():
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, L, d, ps = 3, 4, 2, 70, 8, 16
+    q = rng.standard_normal((B, Hq, d))
+    k = rng.standard_normal((B, Hkv, L, d))
+    v = rng.standard_normal((B, Hkv, L, d))
+    kp, table = _paged_from_contiguous(k, ps, np.random.default_rng(1))
+    vp, table_v = _paged_from_contiguous(v, ps, np.random.default_rng(1))
+    assert np.array_equal(table, table_v)
+    lens = np.array([70, 33, 16])
+    o, lse = oracle.decode_paged(q, kp, vp, table, lens, ps, 0.3)
+    for b in range(B):
+        ref_o, ref_lse = oracle.attention_fwd(q[b:b + 1, :, None, :], k[b:b + 1, :, :lens[b]],
+                                              v[b:b + 1, :, :lens[b]], 0.3, False)
+        np.testing.assert_allclose(o[b], ref_o[0, :, 0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[b], ref_lse[0, :, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_paged_decode_independent_of_page_placement():
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, L, d, ps = 2, 2, 1, 50, 4, 8
+    q = rng.standard_normal((B, Hq, d))
+    k = rng.standard_normal((B, Hkv, L, d))
+    v = rng.standard_normal((B, Hkv, L, d))
+    lens = np.array([50, 21])
+    outs = []
+    for seed in (3, 4):
+        kp, table = _paged_from_contiguous(k, ps, np.random.default_rng(seed))
+        vp, _ = _paged_from_contiguous(v, ps, np.random.default_rng(seed))
+        outs.append(oracle.decode_paged(q, kp, vp, table, lens, ps, 0.5))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+
+
+def test_paged_decode_closed_forms():
+    """Length 0: O = 0, LSE = -inf. Length 1: O = v_0, LSE = scale·k_0·q.
+    Length 2: O = (e^s0 v0 + e^s1 v1) / (e^s0 + e^s1)."""
+    rng = np.random.default_rng(13)
+    Hkv, ps, d = 1, 4, 3
+    pages = rng.standard_normal((3, Hkv, ps, d))
+    vpages = rng.standard_normal((3, Hkv, ps, d))
+    table = np.array([[2, 0], [1, 2], [0, 1]])
+    q = rng.standard_normal((3, 1, d))
+    o, lse = oracle.decode_paged(q, pages, vpages, table, np.array([0, 1, 2]), ps, 0.7)
+    assert np.all(o[0] == 0) and lse[0, 0] == -np.inf
+    k0, v0 = pages[1, 0, 0], vpages[1, 0, 0]
+    np.testing.assert_allclose(o[1, 0], v0, rtol=1e-14)
+    assert abs(lse[1, 0] - 0.7 * (k0 @ q[1, 0])) < 1e-14
+    s0, s1 = 0.7 * (pages[0, 0, 0] @ q[2, 0]), 0.7 * (pages[0, 0, 1] @ q[2, 0])
+    w0, w1 = np.exp(s0), np.exp(s1)
+    np.testing.assert_allclose(o[2, 0], (w0 * vpages[0, 0, 0] + w1 * vpages[0, 0, 1]) / (w0 + w1),
+                               rtol=1e-12)
+    assert abs(lse[2, 0] - np.log(w0 + w1)) < 1e-12
