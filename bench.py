@@ -3,7 +3,7 @@
 Default workload (N=1): the batched multi-head forward B=4, H=16, N=2048,
 d=64, bf16, non-causal. ``--workload`` selects the other workloads
 (fwd_causal_n8192_d128, bwd_causal_n4096_d128, decode_gqa_l4096,
-fwd_f32_single_head). A step is one pass of the workload's hot path through
+decode_paged_gqa_l4096, fwd_f32_single_head). A step is one pass of the workload's hot path through
 the C ABI on inputs already resident in HBM; L2 is flushed (256 MiB write)
 between timed steps unless the inputs exceed L2.
 
@@ -35,12 +35,30 @@ L2_BYTES = 129 << 20
 
 # ----------------------------------------------------------------- workload math
 
-def algorithmic_units(w):
+def make_workload_inputs(w):
+    from workloads import make_inputs, make_paged_inputs
+    return make_paged_inputs(w) if w.kind == "decode_paged" else make_inputs(w)
+
+
+def paged_bytes(w, seq_lens):
+    """Bytes a paged decode must move: each request's K and V rows once, its
+    block-table entries, its length, q and o."""
+    P = w.page_size
+    keys = sum(int(n) for n in seq_lens)
+    blocks = sum((int(n) + P - 1) // P for n in seq_lens)
+    return (2 * w.Hkv * keys * w.d * 2 + 2 * len(seq_lens) * w.Hq * w.d * 2
+            + 4 * (blocks + len(seq_lens)))
+
+
+def algorithmic_units(w, inputs=None):
     """(per-step units, unit name, bound) for a workload.
 
     FLOPs: 2 per multiply-add; the forward has two GEMMs (4·Nq·Nk·d per head,
     causal counts only the visible pairs), the backward five (2.5x the
-    forward). Decode bytes: K and V read once plus q and o."""
+    forward). Decode bytes: K and V read once plus q and o (paged decode:
+    over each request's own length, plus its block-table entries)."""
+    if w.kind == "decode_paged":
+        return paged_bytes(w, inputs["seq_lens"].tolist()), "GB/s", "hbm"
     if w.kind == "decode":
         bytes_ = 2 * w.B * w.Hkv * w.Nk * w.d * 2 + 2 * w.B * w.Hq * w.d * 2
         return bytes_, "GB/s", "hbm"
@@ -138,12 +156,32 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
     """Time the float64 oracle on whole (b, h) heads of the workload until the
     budget is spent; returns (units processed, seconds, description)."""
     import numpy as np
+    import torch
+
     import oracle
     from workloads import to_f64
 
-    units_total, _, _ = algorithmic_units(w)
+    units_total, _, _ = algorithmic_units(w, inputs)
     t0 = time.perf_counter()
     done = 0
+    if w.kind == "decode_paged":
+        lens = inputs["seq_lens"].numpy()
+        table = inputs["block_table"].numpy()
+        kp, vp = inputs["k_pages"], inputs["v_pages"]
+        units = 0
+        for b in range(w.B):
+            # only this request's pages are converted: the pool is shared
+            pages = table[b, :(int(lens[b]) + w.page_size - 1) // w.page_size]
+            idx = torch.as_tensor(pages.astype("int64"))
+            k, v = to_f64(kp[idx]), to_f64(vp[idx])
+            local = np.arange(len(pages), dtype=np.int32)[None, :]
+            oracle.decode_paged(to_f64(inputs["q"][b:b + 1]), k, v, local, lens[b:b + 1],
+                                w.page_size, w.scale)
+            units += paged_bytes(w, lens[b:b + 1].tolist())
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return units, time.perf_counter() - t0, f"{done} of {w.B} requests"
     if w.kind == "decode":
         per_req = units_total / w.B
         for b in range(w.B):
@@ -187,9 +225,8 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    from workloads import make_inputs
-    units, unit, _ = algorithmic_units(w)
-    inputs = make_inputs(w)
+    inputs = make_workload_inputs(w)
+    units, unit, _ = algorithmic_units(w, inputs)
     budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         cpu_oracle_sample(w, inputs, budget / 4)
@@ -220,8 +257,12 @@ METRIC = "attn fwd/bwd TFLOP/s vs GB300 BF16 peak; split-KV decode GB/s vs HBM"
 def workload_config(w, flushed: bool):
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk,
            "d": w.d, "causal": w.causal, "dtype": w.dtype}
-    if w.kind == "decode":
+    if w.kind in ("decode", "decode_paged"):
         cfg["num_splits"] = w.num_splits
+    if w.kind == "decode_paged":
+        cfg["Nk"] = f"per-request lengths uniform on [1, {2 * w.Nk - 1}] (mean {w.Nk})"
+        cfg["page_size"] = w.page_size
+        cfg["pages"] = "pool handed out in a seeded random order"
     cfg["l2"] = ("flushed between timed steps (256 MiB write)" if flushed
                  else "inputs larger than L2 (129 MB); no flush")
     return cfg
@@ -238,7 +279,8 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-KERNEL_SOURCES = {"fwd": "fwd_tc.cu", "bwd": "bwd_tc.cu", "decode": "decode.cu"}
+KERNEL_SOURCES = {"fwd": "fwd_tc.cu", "bwd": "bwd_tc.cu", "decode": "decode.cu",
+                  "decode_paged": "decode.cu"}
 FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
@@ -250,6 +292,8 @@ def kernel_label(w):
         if w.dtype == "bf16" and w.d == 128:
             return "attn_bwd call (row-term preprocess + dK/dV key-tile pass + dQ query-tile pass)"
         return "attn_bwd call (row-term preprocess + main kernel + dQ convert)"
+    if w.kind == "decode_paged":
+        return "attn_decode_paged call (split kernel + merge kernel)"
     return "attn_decode_splitkv call (split kernel + merge kernel)"
 
 
@@ -279,7 +323,6 @@ def run_gpu(args, w):
     import torch.distributed as dist
 
     import online_softmax_tiled_gb300 as ost
-    from workloads import make_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -296,9 +339,9 @@ def run_gpu(args, w):
     ost.lib()
     stream = torch.cuda.current_stream(dev)
 
-    host = make_inputs(w)
+    host = make_workload_inputs(w)
     x = {k: t.to(dev) for k, t in host.items()}
-    units, unit, bound = algorithmic_units(w)
+    units, unit, bound = algorithmic_units(w, host)
     in_bytes = sum(t.numel() * t.element_size() for t in host.values())
     flush = in_bytes < L2_BYTES
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
@@ -319,6 +362,16 @@ def run_gpu(args, w):
                                     w.scale, w.causal, ws, stream)
         launches_per_step = 3
         outs = (dq, dk, dv)
+    elif w.kind == "decode_paged":
+        ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq, w.d, w.num_splits),
+                         dtype=torch.uint8, device=dev)
+        o = torch.empty_like(x["q"])
+        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+        step = lambda: ost.attn_decode_paged(x["q"], x["k_pages"], x["v_pages"],
+                                             x["block_table"], x["seq_lens"], o, lse, w.scale,
+                                             w.num_splits, ws, stream)
+        launches_per_step = 2
+        outs = (o, lse)
     else:
         ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq, w.d, w.num_splits),
                          dtype=torch.uint8, device=dev)

@@ -59,7 +59,8 @@ typedef enum {
   ATTN_ERR_MISALIGNED = -3,      /* a tensor pointer is not 16-byte aligned             */
   ATTN_ERR_WORKSPACE = -4,       /* workspace null or smaller than *_workspace_size()   */
   ATTN_ERR_CUDA = -5,            /* a CUDA runtime call or kernel launch failed         */
-  ATTN_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait ran out                  */
+  ATTN_ERR_DEVICE_TIMEOUT = -6,  /* a bounded device-side wait ran out                  */
+  ATTN_ERR_DEVICE_INDEX = -7     /* a length or page index read on the device was out of range */
 } attn_status;
 
 typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
@@ -144,6 +145,43 @@ ATTN_API attn_status attn_decode_splitkv(const void* q, const void* k_cache, con
                                 void* stream);
 
 /*
+ * Paged, variable-length split-KV decode.
+ *
+ * ML notes (haolingpu.github.io), KV-cache Q&A: the cache is allocated in
+ * fixed-size blocks that a per-request block table maps, like pages through
+ * a page table (PagedAttention); decode steps of different requests are
+ * independent, each reading its own cache. Computes, for every request b
+ * with n_b = seq_lens[b] keys, what attn_decode_splitkv computes on the
+ * contiguous cache gathered from its pages: key t of request b, KV head g,
+ * is row (t % page_size) of head g in page block_table[b*max_pages_per_seq +
+ * t / page_size].
+ *
+ * q [B,Hq,d] bf16; k_pages/v_pages [num_pages, Hkv, page_size, d] bf16;
+ * block_table [B, max_pages_per_seq] int32 and seq_lens [B] int32, DEVICE
+ * memory (read by the kernel, so both may be written by earlier work on
+ * `stream`); o [B,Hq,d] bf16 written; lse [B,Hq] float32 written (may be
+ * NULL). Entries of block_table past ceil(n_b / page_size) are not read.
+ * page_size >= 1 (a multiple of 32 reads each 32-key step with one copy per
+ * tensor; smaller or other sizes with one per page touched); d 64 or 128;
+ * Hq/Hkv <= 8.
+ * A request with n_b = 0 gets O = 0, LSE = -inf. The chunk of split s is
+ * [s*c, min((s+1)*c, n_b)) with c = ceil(n_b / num_splits) rounded up to
+ * a multiple of 32 keys.
+ * Device-side checks: a length outside [0, max_pages_per_seq*page_size] or
+ * a page index outside [0, num_pages) is never dereferenced; the request
+ * (for a bad length) or the split holding the bad index gets no keys, and
+ * attn_sync_status() reports ATTN_ERR_DEVICE_INDEX.
+ * workspace: at least attn_decode_workspace_size(B, Hq, d, num_splits)
+ * bytes, 256-byte aligned.
+ */
+ATTN_API attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int* block_table, const int* seq_lens, void* o,
+                              float* lse, int B, int Hq, int Hkv, int num_pages,
+                              int page_size, int max_pages_per_seq, int d, float scale,
+                              int num_splits, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/*
  * The exact (o, m, l) merge on its own (ML notes, split-K notes; the
  * attention-residuals lab, "Phase 2: merge the live partial exactly").
  *
@@ -198,7 +236,9 @@ ATTN_API const char* attn_status_string(attn_status s);
 /*
  * Synchronise `stream`, then report (and clear) the library's device error
  * word: ATTN_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the
- * last check, ATTN_ERR_CUDA if the stream reports a CUDA error, else ATTN_OK.
+ * last check, else ATTN_ERR_DEVICE_INDEX if a paged decode met an
+ * out-of-range length or page index; ATTN_ERR_CUDA if the stream reports a
+ * CUDA error; else ATTN_OK.
  */
 ATTN_API attn_status attn_sync_status(void* stream);
 

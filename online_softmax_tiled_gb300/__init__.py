@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     AttnError,
     attn_bwd,
     attn_bwd_workspace_size,
+    attn_decode_paged,
     attn_decode_splitkv,
     attn_decode_splitkv_noalloc,
     attn_decode_workspace_size,
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     attn_sync_status,
     backward,
     decode,
+    decode_paged,
     forward,
     lib,
 )

@@ -22,7 +22,7 @@ ATTN_BF16 = 1
 _STATUS_NAMES = {
     0: "ATTN_OK", -1: "ATTN_ERR_INVALID_ARG", -2: "ATTN_ERR_UNSUPPORTED",
     -3: "ATTN_ERR_MISALIGNED", -4: "ATTN_ERR_WORKSPACE", -5: "ATTN_ERR_CUDA",
-    -6: "ATTN_ERR_DEVICE_TIMEOUT",
+    -6: "ATTN_ERR_DEVICE_TIMEOUT", -7: "ATTN_ERR_DEVICE_INDEX",
 }
 
 
@@ -46,6 +46,9 @@ _SIGNATURES = {
     "attn_decode_splitkv": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 +
                             [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                              ctypes.c_void_p]),
+    "attn_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 7 +
+                          [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                           ctypes.c_void_p]),
     "attn_merge_partials": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
                             [ctypes.c_void_p]),
     "attn_decode_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 +
@@ -166,6 +169,24 @@ def attn_decode_splitkv_noalloc(q, k_cache, v_cache, o, lse, scale: float, num_s
     _check(st, "attn_decode_splitkv_noalloc")
 
 
+def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale: float,
+                      num_splits: int, workspace, stream=None):
+    """q [B,Hq,d] bf16; pages [num_pages,Hkv,page_size,d] bf16; block_table
+    [B,max_pages] and seq_lens [B] int32 on the device; o [B,Hq,d] bf16;
+    lse [B,Hq] float32 or None."""
+    _device_contig(q, k_pages, v_pages, block_table, seq_lens, o, lse, workspace)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_table and seq_lens must be int32")
+    B, Hq, d = q.shape
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                 _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, num_pages,
+                                 page_size, block_table.shape[1], d, float(scale),
+                                 int(num_splits), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "attn_decode_paged")
+
+
 def attn_merge_partials(o_part, m_part, l_part, o, lse, stream=None):
     """o_part [rows,S,d], m_part/l_part [rows,S] float32 -> o [rows,d], lse [rows]."""
     _device_contig(o_part, m_part, l_part, o, lse)
@@ -219,4 +240,19 @@ def decode(q, k_cache, v_cache, num_splits: int, scale: float | None = None, str
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     attn_decode_splitkv(q, k_cache, v_cache, o, lse, scale, num_splits, workspace, stream)
+    return o, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, num_splits: int,
+                 scale: float | None = None, stream=None, workspace=None):
+    """Paged, variable-length split-KV decode: O [B,Hq,d] bf16, LSE [B,Hq] float32."""
+    B, Hq, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(B, Hq, d, num_splits),
+                                dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale, num_splits,
+                      workspace, stream)
     return o, lse

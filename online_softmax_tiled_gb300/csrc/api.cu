@@ -68,6 +68,7 @@ const char* attn_status_string(attn_status s) {
     case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_DEVICE_INDEX: return "out-of-range length or page index read on the device";
   }
   return "unknown status";
 }
@@ -163,6 +164,47 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
   return from_cuda(launch_merge(m));
 }
 
+attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int* block_table, const int* seq_lens, void* o, float* lse,
+                              int B, int Hq, int Hkv, int num_pages, int page_size,
+                              int max_pages_per_seq, int d, float scale, int num_splits,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || page_size <= 0 ||
+      max_pages_per_seq <= 0 || d <= 0 || num_splits <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !o) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
+  if (num_splits > 65535 || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  // key positions and page row offsets are 32-bit inside the kernel
+  if ((long long)max_pages_per_seq * page_size > (1LL << 30) ||
+      (long long)num_pages * Hkv * page_size > (1LL << 40))
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o) ||
+      (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const DecodeLayout lay = decode_layout(B, Hq, d, num_splits);
+  if (!workspace || ws_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  char* ws = static_cast<char*>(workspace);
+  DecodeArgs a{q, k_pages, v_pages, o, lse, B, Hq, Hkv, 0, d, scale, num_splits,
+               reinterpret_cast<float*>(ws + lay.o_part), reinterpret_cast<float*>(ws + lay.m_part),
+               reinterpret_cast<float*>(ws + lay.l_part), static_cast<cudaStream_t>(stream)};
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.max_pages = max_pages_per_seq;
+  cudaError_t e = launch_decode_split(a);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  MergeArgs m{a.o_part, a.m_part, a.l_part, o, lse, B * Hq, num_splits, d, ATTN_BF16, a.stream};
+  return from_cuda(launch_merge(m));
+}
+
 attn_status attn_merge_partials(const float* o_part, const float* m_part, const float* l_part,
                                 void* o, float* lse, int rows, int num_splits, int d,
                                 attn_dtype out_dt, void* stream) {
@@ -183,6 +225,7 @@ attn_status attn_sync_status(void* stream) {
       take_error_fwd_tc() | take_error_bwd_tc() | take_error_bwd_dq() | take_error_decode();
   if (w == 0xffffffffu) return ATTN_ERR_CUDA;
   if (w & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
+  if (w & kErrBadIndex) return ATTN_ERR_DEVICE_INDEX;
   return ATTN_OK;
 }
 

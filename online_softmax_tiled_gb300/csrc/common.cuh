@@ -15,9 +15,10 @@ namespace attn {
 // Error word. Each translation unit owns one (kernels in different units are
 // compiled without relocatable device code, so a single shared __device__
 // variable is not possible); the host polls all of them in attn_sync_status.
-// Bits: 1 = a bounded wait ran out.
+// Bits: 1 = a bounded wait ran out; 2 = an index read from device memory (a
+// paged-decode length or block-table entry) was out of range.
 // ----------------------------------------------------------------------------
-enum : uint32_t { kErrTimeout = 1u };
+enum : uint32_t { kErrTimeout = 1u, kErrBadIndex = 2u };
 
 #define ATTN_DEFINE_ERROR_WORD(fn_name)                                          \
   static __device__ uint32_t g_attn_err_word;                                  \

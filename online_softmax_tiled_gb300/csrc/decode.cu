@@ -20,6 +20,15 @@
 // shared loads cover whole 128-byte rows without bank conflicts. Each 8-lane
 // group runs its own online softmax over its keys; the 16 groups of the CTA
 // are merged with the same exact rule at the end.
+//
+// Paged, variable-length decode (ML notes, prefill/decode and the KV cache:
+// the cache lives in fixed-size blocks reached through a per-request block
+// table): the same kernel with request b's length read from seq_lens[b] and
+// key t read from page block_table[b][t / page_size]. Each 32-key stage is
+// filled by one bulk copy per page it touches (rows are 128 or 256 bytes, so
+// every row start is 16-byte aligned); splits start on multiples of 32 keys,
+// so with 32 | page_size that is one copy per tensor, as for a contiguous
+// cache.
 
 #include <mutex>
 
@@ -47,12 +56,20 @@ constexpr size_t decode_smem_bytes() {
   return ring > merge ? ring : merge;
 }
 
-template <int D, int G>
+// Paged cache: pages [num_pages][Hkv][page_size][D]; block_table
+// [B][max_pages]; seq_lens [B].
+struct PagedKV {
+  const int* block_table;
+  const int* seq_lens;
+  int num_pages, page_size, max_pages;
+};
+
+template <int D, int G, bool kPaged>
 __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
-                    int L, int S, float scale) {
+                    int L, int S, float scale, PagedKV pg) {
   constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
   constexpr int kRowBytes = D * 2;
   constexpr int kStageBytes = kStageKeys * kRowBytes;
@@ -67,15 +84,6 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
-  const int chunk = (L + S - 1) / S;
-  const int key_begin = min(L, s * chunk);
-  const int key_end = min(L, key_begin + chunk);
-  const int nkeys = key_end - key_begin;
-  const int nstages = (nkeys + kStageKeys - 1) / kStageKeys;
-
-  const size_t kv_off = (size_t(b) * Hkv + g) * size_t(L) * D;
-  const uint8_t* kg = reinterpret_cast<const uint8_t*>(k + kv_off) + size_t(key_begin) * kRowBytes;
-  const uint8_t* vg = reinterpret_cast<const uint8_t*>(v + kv_off) + size_t(key_begin) * kRowBytes;
 
   if (tid == 0) {
     abort_flag = 0;
@@ -86,15 +94,64 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   // (q, the KV cache, the partials a previous merge may still be reading)
   // comes after the preceding grid has completed.
   pdl_wait_primary();
-  __syncthreads();
 
+  // This CTA's keys [key_begin, key_end). Contiguous cache: chunk
+  // ceil(L / S). Paged: the request's own length, chunks rounded up to 32
+  // keys; an out-of-range length empties the request and an out-of-range
+  // page index this chunk (both flagged; neither is dereferenced).
+  int Lb = L, chunk;
+  if (kPaged) {
+    Lb = pg.seq_lens[b];
+    if (Lb < 0 || Lb > pg.max_pages * pg.page_size) Lb = -1;
+    chunk = Lb > 0 ? (((Lb + S - 1) / S + kStageKeys - 1) / kStageKeys) * kStageKeys : 0;
+  } else {
+    chunk = (L + S - 1) / S;
+  }
+  const int key_begin = max(0, min(Lb, s * chunk));
+  const int key_end = max(0, min(Lb, key_begin + chunk));
+  bool bad = kPaged && Lb < 0;
+  if (kPaged && key_end > key_begin) {
+    // every page index of the chunk, checked by the whole CTA before use
+    const int p_end = (key_end + pg.page_size - 1) / pg.page_size;
+    for (int p = key_begin / pg.page_size + tid; p < p_end; p += kThreads) {
+      const int page = pg.block_table[size_t(b) * pg.max_pages + p];
+      bad |= page < 0 || page >= pg.num_pages;
+    }
+  }
+  // (also orders the barrier initialisation before any use)
+  bad = __syncthreads_or(bad);
+  if (bad && tid == 0) attn_flag_error(kErrBadIndex);
+  const int nkeys = bad ? 0 : key_end - key_begin;
+  const int nstages = (nkeys + kStageKeys - 1) / kStageKeys;
+
+  // Element offset of key t of (b, g) in the K and V arrays.
+  const size_t head_off = kPaged ? size_t(g) * pg.page_size * D
+                                 : (size_t(b) * Hkv + g) * size_t(L) * D;
+  const size_t page_elems = size_t(Hkv) * pg.page_size * D;     // paged only
+  const int* table_row = kPaged ? pg.block_table + size_t(b) * pg.max_pages : nullptr;
   auto issue = [&](int st) {
     const int buf = st % kStages;
+    const int t0 = key_begin + st * kStageKeys;
     const int rows = min(kStageKeys, nkeys - st * kStageKeys);
-    const uint32_t bytes = uint32_t(rows) * kRowBytes;
-    mbar_arrive_expect_tx(&full_bar[buf], 2 * bytes);
-    bulk_g2s(sK + buf * kStageBytes, kg + size_t(st) * kStageBytes, bytes, &full_bar[buf]);
-    bulk_g2s(sV + buf * kStageBytes, vg + size_t(st) * kStageBytes, bytes, &full_bar[buf]);
+    mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
+    if (kPaged) {
+      // one copy per page the stage touches (one when 32 | page_size)
+      for (int t = t0, r = 0; r < rows;) {
+        const int in_page = t % pg.page_size;
+        const int seg = min(rows - r, pg.page_size - in_page);
+        const size_t off = head_off + size_t(table_row[t / pg.page_size]) * page_elems +
+                           size_t(in_page) * D;
+        const uint32_t dst = buf * kStageBytes + r * kRowBytes;
+        bulk_g2s(sK + dst, k + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
+        bulk_g2s(sV + dst, v + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
+        t += seg;
+        r += seg;
+      }
+    } else {
+      const size_t off = head_off + size_t(t0) * D;
+      bulk_g2s(sK + buf * kStageBytes, k + off, uint32_t(rows) * kRowBytes, &full_bar[buf]);
+      bulk_g2s(sV + buf * kStageBytes, v + off, uint32_t(rows) * kRowBytes, &full_bar[buf]);
+    }
   };
   int issued = 0;  // meaningful in thread 0 only
   if (tid == 0)
@@ -348,10 +405,10 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
   if (lse != nullptr && lane == 0) lse[row] = empty ? -INFINITY : mx + logf(l);
 }
 
-template <int D, int G>
+template <int D, int G, bool kPaged>
 cudaError_t launch_split_t(const DecodeArgs& a) {
   const size_t smem = decode_smem_bytes<D, G>();
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, kPaged>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -364,20 +421,21 @@ cudaError_t launch_split_t(const DecodeArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G>,
+  const PagedKV pg{a.block_table, a.seq_lens, a.num_pages, a.page_size, a.max_pages};
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, kPaged>,
                             static_cast<const __nv_bfloat16*>(a.q),
                             static_cast<const __nv_bfloat16*>(a.k),
                             static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part,
-                            a.Hq, a.Hkv, a.L, a.num_splits, a.scale);
+                            a.Hq, a.Hkv, a.L, a.num_splits, a.scale, pg);
 }
 
-template <int D>
+template <int D, bool kPaged>
 cudaError_t launch_split_d(const DecodeArgs& a) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_split_t<D, 1>(a);
-    case 2: return launch_split_t<D, 2>(a);
-    case 4: return launch_split_t<D, 4>(a);
-    case 8: return launch_split_t<D, 8>(a);
+    case 1: return launch_split_t<D, 1, kPaged>(a);
+    case 2: return launch_split_t<D, 2, kPaged>(a);
+    case 4: return launch_split_t<D, 4, kPaged>(a);
+    case 8: return launch_split_t<D, 8, kPaged>(a);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -385,7 +443,9 @@ cudaError_t launch_split_d(const DecodeArgs& a) {
 }  // namespace
 
 cudaError_t launch_decode_split(const DecodeArgs& a) {
-  return a.d == 64 ? launch_split_d<64>(a) : launch_split_d<128>(a);
+  if (a.block_table != nullptr)
+    return a.d == 64 ? launch_split_d<64, true>(a) : launch_split_d<128, true>(a);
+  return a.d == 64 ? launch_split_d<64, false>(a) : launch_split_d<128, false>(a);
 }
 
 cudaError_t launch_merge(const MergeArgs& a) {

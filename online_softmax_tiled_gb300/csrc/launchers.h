@@ -56,6 +56,12 @@ struct DecodeArgs {
   float* m_part;     // [B*Hq, S]
   float* l_part;     // [B*Hq, S]
   cudaStream_t stream;
+  // Paged cache (block_table != nullptr): k, v are pages
+  // [num_pages, Hkv, page_size, d]; request b holds seq_lens[b] keys, key t
+  // in page block_table[b * max_pages + t / page_size]. L is unused.
+  const int* block_table = nullptr;
+  const int* seq_lens = nullptr;
+  int num_pages = 0, page_size = 0, max_pages = 0;
 };
 
 struct MergeArgs {

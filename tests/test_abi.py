@@ -31,8 +31,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = set(_declared_functions())
     assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_decode_splitkv",
-            "attn_decode_workspace_size", "attn_merge_partials", "attn_status_string",
-            "attn_sync_status"} <= names
+            "attn_decode_workspace_size", "attn_decode_paged", "attn_merge_partials",
+            "attn_status_string", "attn_sync_status"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         s = lib.attn_status_string(code)
         assert s and s != b"unknown status"
     assert lib.attn_status_string(42) == b"unknown status"
@@ -122,6 +122,26 @@ def test_decode_rejects_before_launch(lib):
     assert call(L=0) == INVALID
     assert call(ws_bytes=100) == WORKSPACE
     assert call(q=P + 8) == MISALIGNED
+
+
+def test_decode_paged_rejects_before_launch(lib):
+    def call(B=2, Hq=8, Hkv=2, num_pages=16, page_size=64, max_pages=4, d=128, S=4, ws=P,
+             ws_bytes=None, q=P, table=P, lens=P, kp=P):
+        need = lib.attn_decode_workspace_size(B, Hq, d, S) if ws_bytes is None else ws_bytes
+        return lib.attn_decode_paged(q, kp, P, table, lens, P, P, B, Hq, Hkv, num_pages,
+                                     page_size, max_pages, d, 0.1, S, ws, need, None)
+    assert call(page_size=0) == INVALID
+    assert call(num_pages=0) == INVALID
+    assert call(max_pages=0) == INVALID
+    assert call(table=None) == INVALID
+    assert call(lens=None) == INVALID
+    assert call(Hq=6, Hkv=4) == INVALID
+    assert call(Hq=32, Hkv=2) == UNSUPPORTED     # group of 16
+    assert call(d=96) == UNSUPPORTED
+    assert call(max_pages=1 << 20, page_size=2048) == UNSUPPORTED  # 2^31 key positions
+    assert call(ws_bytes=100) == WORKSPACE
+    assert call(kp=P + 8) == MISALIGNED
+    assert call(table=P + 2) == MISALIGNED
 
 
 def test_merge_rejects_before_launch(lib):

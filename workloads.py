@@ -8,6 +8,13 @@ Recipe: one CPU ``torch.Generator`` seeded per workload; float32 N(0, 1)
 draws in the order Q, K, V, then dO for a backward workload; each tensor is
 then cast to the workload's dtype (bf16 by round-to-nearest-even). Both the
 GPU path and the oracle see exactly these cast values.
+
+Paged decode: per-request lengths uniform on [1, 2·Nk − 1] (mean Nk) unless
+given; the pool holds exactly the pages the requests need plus a few spare
+ones, drawn N(0, 1) as [num_pages, Hkv, page_size, d] for K then V, and the
+pages are handed out to the requests in a random order (a seeded
+permutation), so that logically consecutive blocks sit at scattered physical
+addresses. Block-table entries past a request's last block are -1.
 """
 
 from __future__ import annotations
@@ -32,6 +39,7 @@ class Workload:
     causal: bool = False
     num_splits: int = 1
     seed: int = 0
+    page_size: int = 0  # paged decode only: tokens per KV block
 
     @property
     def scale(self) -> float:
@@ -52,6 +60,10 @@ WORKLOADS = {
                                       "bf16", causal=True),
     "decode_gqa_l4096": Workload("decode_gqa_l4096", "decode", 64, 32, 8, 1, 4096, 128, "bf16",
                                  num_splits=16),
+    # The GQA decode shape over a paged cache of 16-token blocks, with ragged
+    # request lengths of mean 4096.
+    "decode_paged_gqa_l4096": Workload("decode_paged_gqa_l4096", "decode_paged", 64, 32, 8, 1,
+                                       4096, 128, "bf16", num_splits=16, page_size=16),
 }
 
 
@@ -76,6 +88,35 @@ def make_inputs(w: Workload, *, Hkv: int | None = None, generator_seed: int | No
     if w.kind == "bwd":
         out["do"] = torch.randn(q_shape, generator=g, dtype=torch.float32)
     return {k: t.to(w.torch_dtype) for k, t in out.items()}
+
+
+def make_paged_inputs(w: Workload, seq_lens=None, spare_pages: int = 3):
+    """Seeded CPU tensors for a paged decode workload.
+
+    q [B, Hq, d]; k_pages, v_pages [num_pages, Hkv, page_size, d];
+    block_table [B, max_pages] int32 (-1 past each request's blocks);
+    seq_lens [B] int32. ``seq_lens`` overrides the drawn lengths.
+    """
+    g = torch.Generator().manual_seed(w.seed)
+    P = w.page_size
+    if seq_lens is None:
+        seq_lens = torch.randint(1, 2 * w.Nk, (w.B,), generator=g)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32)
+    blocks = [(int(n) + P - 1) // P for n in seq_lens]
+    max_pages = max(1, max(blocks))
+    num_pages = sum(blocks) + spare_pages
+    q = torch.randn((w.B, w.Hq, w.d), generator=g, dtype=torch.float32)
+    kp = torch.randn((num_pages, w.Hkv, P, w.d), generator=g, dtype=torch.float32)
+    vp = torch.randn((num_pages, w.Hkv, P, w.d), generator=g, dtype=torch.float32)
+    order = torch.randperm(num_pages, generator=g)
+    table = torch.full((w.B, max_pages), -1, dtype=torch.int32)
+    nxt = 0
+    for b, nb in enumerate(blocks):
+        table[b, :nb] = order[nxt:nxt + nb].to(torch.int32)
+        nxt += nb
+    dt = w.torch_dtype
+    return {"q": q.to(dt), "k_pages": kp.to(dt), "v_pages": vp.to(dt), "block_table": table,
+            "seq_lens": seq_lens}
 
 
 def random_like_shape(shape, dtype: torch.dtype, seed: int, scale: float = 1.0):
