@@ -164,9 +164,12 @@ ATTN_API attn_status attn_decode_splitkv(const void* q, const void* k_cache, con
  * page_size >= 1 (a multiple of 32 reads each 32-key step with one copy per
  * tensor; smaller or other sizes with one per page touched); d 64 or 128;
  * Hq/Hkv <= 8.
- * A request with n_b = 0 gets O = 0, LSE = -inf. The chunk of split s is
- * [s*c, min((s+1)*c, n_b)) with c = ceil(n_b / num_splits) rounded up to
- * a multiple of 32 keys.
+ * A request with n_b = 0 gets O = 0, LSE = -inf. Chunks have one length for
+ * all requests, c = ceil(max_pages_per_seq * page_size / num_splits)
+ * rounded up to a multiple of 32 keys; request b uses its own number of
+ * splits, ceil(n_b / c) <= num_splits, split s covering keys
+ * [s*c, min((s+1)*c, n_b)), so every split carries about the same work
+ * whatever the mix of lengths.
  * Device-side checks: a length outside [0, max_pages_per_seq*page_size] or
  * a page index outside [0, num_pages) is never dereferenced; the request
  * (for a bad length) or the split holding the bad index gets no keys, and

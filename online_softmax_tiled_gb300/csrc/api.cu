@@ -148,6 +148,8 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
   if (num_splits > 65535 || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  // work items (request, KV head, chunk) are numbered in 32 bits
+  if (1LL * B * Hkv * num_splits > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       (lse && !aligned16(lse)))
     return ATTN_ERR_MISALIGNED;
@@ -160,8 +162,7 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
                reinterpret_cast<float*>(ws + lay.l_part), static_cast<cudaStream_t>(stream)};
   cudaError_t e = launch_decode_split(a);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  MergeArgs m{a.o_part, a.m_part, a.l_part, o, lse, B * Hq, num_splits, d, ATTN_BF16, a.stream};
-  return from_cuda(launch_merge(m));
+  return from_cuda(launch_merge(decode_merge_args(a)));
 }
 
 attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
@@ -179,6 +180,8 @@ attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
   if (num_splits > 65535 || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  // work items (request, KV head, chunk) are numbered in 32 bits
+  if (1LL * B * Hkv * num_splits > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
   // key positions and page row offsets are 32-bit inside the kernel
   if ((long long)max_pages_per_seq * page_size > (1LL << 30) ||
       (long long)num_pages * Hkv * page_size > (1LL << 40))
@@ -201,8 +204,7 @@ attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_
   a.max_pages = max_pages_per_seq;
   cudaError_t e = launch_decode_split(a);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  MergeArgs m{a.o_part, a.m_part, a.l_part, o, lse, B * Hq, num_splits, d, ATTN_BF16, a.stream};
-  return from_cuda(launch_merge(m));
+  return from_cuda(launch_merge(decode_merge_args(a)));
 }
 
 attn_status attn_merge_partials(const float* o_part, const float* m_part, const float* l_part,

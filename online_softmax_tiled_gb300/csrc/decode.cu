@@ -5,9 +5,9 @@
 // leaves its maximum score m_s, un-normalised denominator
 // l_s = Σ exp(s - m_s) and un-normalised output o_s = Σ exp(s - m_s) v in
 // global scratch, and a second kernel rescales every chunk by exp(m_s - m)
-// onto the common maximum m and merges them exactly, in any order. An empty
-// chunk has m_s = -inf and carries zero mass (attention-residuals kernel
-// lab, manishklach.github.io, "Phase 2").
+// onto the common maximum m and merges them exactly, in any order. A chunk
+// with no keys carries zero mass (attention-residuals kernel lab,
+// manishklach.github.io, "Phase 2"): it is simply left out of the merge.
 //
 // Split kernel. Decode is bound by reading the KV cache once (about 4 flops
 // per byte), so it runs on the FMA pipes, not the tensor cores. One CTA owns
@@ -21,14 +21,21 @@
 // group runs its own online softmax over its keys; the 16 groups of the CTA
 // are merged with the same exact rule at the end.
 //
-// Paged, variable-length decode (ML notes, prefill/decode and the KV cache:
-// the cache lives in fixed-size blocks reached through a per-request block
-// table): the same kernel with request b's length read from seq_lens[b] and
-// key t read from page block_table[b][t / page_size]. Each 32-key stage is
-// filled by one bulk copy per page it touches (rows are 128 or 256 bytes, so
-// every row start is 16-byte aligned); splits start on multiples of 32 keys,
-// so with 32 | page_size that is one copy per tensor, as for a contiguous
-// cache.
+// Paged, variable-length decode (ML notes, KV-cache Q&A: the cache lives in
+// fixed-size blocks reached through a per-request block table, as pages
+// through a page table): the same kernel with request b's length read from
+// seq_lens[b] and key t read from page block_table[b][t / page_size].
+// Chunks have one length c for all requests (the table's capacity over the
+// split count, rounded up to 32 keys), so request b uses its own number of
+// splits, ceil(n_b / c), every non-empty chunk carries about the same work
+// and the CTAs of chunks past a request's end return at once (the merge
+// reads only a request's own chunks). A CTA fetches its request's length and
+// all block-table entries of its chunk in one round of independent loads,
+// keeps the entries in shared memory and range-checks every one before any
+// page is read. Each 32-key stage is filled by one bulk copy per page it
+// touches (rows are 128 or 256 bytes, so every row start is 16-byte
+// aligned); chunks start on multiples of 32 keys, so with 32 | page_size
+// that is one copy per tensor, as for a contiguous cache.
 
 #include <mutex>
 
@@ -44,6 +51,7 @@ namespace {
 constexpr int kThreads = 128;     // 4 warps, 16 key groups of 8 lanes
 constexpr int kStageKeys = 32;    // keys per pipeline stage
 constexpr int kStages = 4;
+constexpr int kChunkPagesCached = 256;   // block-table entries of a chunk kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -69,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
-                    int L, int S, float scale, PagedKV pg) {
+                    int L, int S, int chunk, float scale, PagedKV pg) {
   constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
   constexpr int kRowBytes = D * 2;
   constexpr int kStageBytes = kStageKeys * kRowBytes;
@@ -80,6 +88,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   uint8_t* sV = smem + kStages * kStageBytes;
   __shared__ uint64_t full_bar[kStages];
   __shared__ int abort_flag;
+  __shared__ int chunk_pages[kPaged ? kChunkPagesCached : 1];
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -95,40 +104,71 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   // comes after the preceding grid has completed.
   pdl_wait_primary();
 
-  // This CTA's keys [key_begin, key_end). Contiguous cache: chunk
-  // ceil(L / S). Paged: the request's own length, chunks rounded up to 32
-  // keys; an out-of-range length empties the request and an out-of-range
-  // page index this chunk (both flagged; neither is dereferenced).
-  int Lb = L, chunk;
+  // This CTA's keys [key_begin, key_end): chunk s of its request.
+  const int max_len = kPaged ? pg.max_pages * pg.page_size : L;
+  const int* table_row = kPaged ? pg.block_table + size_t(b) * pg.max_pages : nullptr;
+  int Lb = L;
+  bool bad = false;
+  int p_first = 0;
   if (kPaged) {
+    // The length and every table entry the chunk can touch, as independent
+    // loads; entries are checked once the length says which ones are used.
     Lb = pg.seq_lens[b];
-    if (Lb < 0 || Lb > pg.max_pages * pg.page_size) Lb = -1;
-    chunk = Lb > 0 ? (((Lb + S - 1) / S + kStageKeys - 1) / kStageKeys) * kStageKeys : 0;
-  } else {
-    chunk = (L + S - 1) / S;
-  }
-  const int key_begin = max(0, min(Lb, s * chunk));
-  const int key_end = max(0, min(Lb, key_begin + chunk));
-  bool bad = kPaged && Lb < 0;
-  if (kPaged && key_end > key_begin) {
-    // every page index of the chunk, checked by the whole CTA before use
-    const int p_end = (key_end + pg.page_size - 1) / pg.page_size;
-    for (int p = key_begin / pg.page_size + tid; p < p_end; p += kThreads) {
-      const int page = pg.block_table[size_t(b) * pg.max_pages + p];
-      bad |= page < 0 || page >= pg.num_pages;
+    const int nominal = s * chunk;
+    p_first = nominal / pg.page_size;
+    const int p_cap = min(pg.max_pages, (min(max_len, nominal + chunk) + pg.page_size - 1) /
+                                            pg.page_size);
+    int ent[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = p_first + tid + i * kThreads;
+      ent[i] = p < p_cap ? table_row[p] : 0;
+    }
+    if (Lb < 0 || Lb > max_len) {
+      if (s == 0 && g == 0 && tid == 0) attn_flag_error(kErrBadIndex);
+      Lb = 0;
+    }
+    const int p_used = (min(Lb, nominal + chunk) + pg.page_size - 1) / pg.page_size;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = p_first + tid + i * kThreads;
+      if (p < p_used) bad |= ent[i] < 0 || ent[i] >= pg.num_pages;
+      if (tid + i * kThreads < kChunkPagesCached) chunk_pages[tid + i * kThreads] = ent[i];
+    }
+    // chunks of more than 4 x kThreads pages (pages far smaller than the
+    // chunk): the rest checked straight from the table
+    for (int p = p_first + 4 * kThreads + tid; p < p_used; p += kThreads) {
+      const int e = table_row[p];
+      bad |= e < 0 || e >= pg.num_pages;
     }
   }
-  // (also orders the barrier initialisation before any use)
+  const int key_begin = min(Lb, s * chunk);
+  const int key_end = min(Lb, key_begin + chunk);
+  // (also orders the barrier initialisation and the cached entries before use)
   bad = __syncthreads_or(bad);
-  if (bad && tid == 0) attn_flag_error(kErrBadIndex);
-  const int nkeys = bad ? 0 : key_end - key_begin;
+  if (bad) {
+    // a page index out of range: the chunk reads nothing and leaves no mass
+    if (tid == 0) attn_flag_error(kErrBadIndex);
+    if (tid < G) {
+      const size_t row = size_t(b) * Hq + g * G + tid;
+      m_part[row * S + s] = -INFINITY;
+      l_part[row * S + s] = 0.f;
+    }
+    return;
+  }
+  const int nkeys = key_end - key_begin;
+  // past the request's end: the merge never reads this chunk
+  if (nkeys <= 0) return;
   const int nstages = (nkeys + kStageKeys - 1) / kStageKeys;
 
   // Element offset of key t of (b, g) in the K and V arrays.
   const size_t head_off = kPaged ? size_t(g) * pg.page_size * D
                                  : (size_t(b) * Hkv + g) * size_t(L) * D;
   const size_t page_elems = size_t(Hkv) * pg.page_size * D;     // paged only
-  const int* table_row = kPaged ? pg.block_table + size_t(b) * pg.max_pages : nullptr;
+  auto page_of = [&](int t) {
+    const int i = t / pg.page_size - p_first;
+    return i < kChunkPagesCached ? chunk_pages[i] : table_row[t / pg.page_size];
+  };
   auto issue = [&](int st) {
     const int buf = st % kStages;
     const int t0 = key_begin + st * kStageKeys;
@@ -139,8 +179,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
       for (int t = t0, r = 0; r < rows;) {
         const int in_page = t % pg.page_size;
         const int seg = min(rows - r, pg.page_size - in_page);
-        const size_t off = head_off + size_t(table_row[t / pg.page_size]) * page_elems +
-                           size_t(in_page) * D;
+        const size_t off = head_off + size_t(page_of(t)) * page_elems + size_t(in_page) * D;
         const uint32_t dst = buf * kStageBytes + r * kRowBytes;
         bulk_g2s(sK + dst, k + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
         bulk_g2s(sV + dst, v + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
@@ -339,14 +378,17 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 }
 
 // One warp per output row; lane owns float4 column groups lane, lane+32, ...
-// The partials of a row are fetched eight at a time with independent loads
-// (their weights exp(m_t - m) are computed once per lane first), so a row
-// costs about S/8 memory round trips rather than S.
+// A row merges its first nv partials: all S for a plain merge, else the
+// chunks that hold keys of its request (ceil(n / chunk), n its length; a
+// length outside [0, max_len] counts as 0). The partials are fetched eight
+// at a time with independent loads (their weights exp(m_t - m) computed
+// once per lane first), so a row costs about nv/8 memory round trips.
 template <typename TOut>
 __global__ void __launch_bounds__(256)
 merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
              const float* __restrict__ l_part, TOut* __restrict__ o, float* __restrict__ lse,
-             int rows, int S, int d) {
+             int rows, int S, int d, const int* __restrict__ seq_lens, int Hq, int len,
+             int max_len, int chunk) {
   constexpr int kBatch = 8;
   // Launched as a programmatic dependent: the partials are read only after
   // the preceding (split) grid has completed. Whatever follows may launch
@@ -356,16 +398,21 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
+  int nv = S;
+  if (chunk > 0) {
+    int n = seq_lens != nullptr ? seq_lens[row / Hq] : len;
+    if (n < 0 || n > max_len) n = 0;
+    nv = min(S, (n + chunk - 1) / chunk);
+  }
   const float* mr = m_part + size_t(row) * S;
   const float* lr = l_part + size_t(row) * S;
   float mx = -INFINITY;
-  for (int t = lane; t < S; t += 32) mx = fmaxf(mx, mr[t]);
+  for (int t = lane; t < nv; t += 32) mx = fmaxf(mx, mr[t]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  // lane t (< S) holds the weight of partial t; rows with S > 32 loop
   float l = 0.f;
   if (mx != -INFINITY)
-    for (int t = lane; t < S; t += 32) {
+    for (int t = lane; t < nv; t += 32) {
       const float mt = mr[t];
       if (mt != -INFINITY) l = fmaf(expf(mt - mx), lr[t], l);
     }
@@ -378,13 +425,13 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
   for (int c4 = lane; c4 < d4; c4 += 32) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!empty)
-      for (int t0 = 0; t0 < S; t0 += kBatch) {
+      for (int t0 = 0; t0 < nv; t0 += kBatch) {
         float4 x[kBatch];
         float w[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int t = t0 + u;
-          const float mt = t < S ? mr[t] : -INFINITY;
+          const float mt = t < nv ? mr[t] : -INFINITY;
           w[u] = mt == -INFINITY ? 0.f : expf(mt - mx);
           x[u] = w[u] != 0.f ? prow[size_t(t) * d4 + c4] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -426,7 +473,7 @@ cudaError_t launch_split_t(const DecodeArgs& a) {
                             static_cast<const __nv_bfloat16*>(a.q),
                             static_cast<const __nv_bfloat16*>(a.k),
                             static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part,
-                            a.Hq, a.Hkv, a.L, a.num_splits, a.scale, pg);
+                            a.Hq, a.Hkv, a.L, a.num_splits, decode_chunk(a), a.scale, pg);
 }
 
 template <int D, bool kPaged>
@@ -463,9 +510,11 @@ cudaError_t launch_merge(const MergeArgs& a) {
   cfg.numAttrs = 1;
   if (a.out_dt == ATTN_F32)
     return cudaLaunchKernelEx(&cfg, merge_kernel<float>, a.o_part, a.m_part, a.l_part,
-                              static_cast<float*>(a.o), a.lse, a.rows, a.num_splits, a.d);
+                              static_cast<float*>(a.o), a.lse, a.rows, a.num_splits, a.d,
+                              a.seq_lens, a.Hq, a.len, a.max_len, a.chunk);
   return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, a.o_part, a.m_part, a.l_part,
-                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.rows, a.num_splits, a.d);
+                            static_cast<__nv_bfloat16*>(a.o), a.lse, a.rows, a.num_splits, a.d,
+                            a.seq_lens, a.Hq, a.len, a.max_len, a.chunk);
 }
 
 }  // namespace attn

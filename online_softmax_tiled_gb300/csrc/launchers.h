@@ -73,7 +73,35 @@ struct MergeArgs {
   int rows, num_splits, d;
   attn_dtype out_dt;
   cudaStream_t stream;
+  // Decode partials (chunk > 0): row r merges only the chunks that hold keys
+  // of its request, ceil(n / chunk) of them, with n = seq_lens[r / Hq] (or
+  // `len` when seq_lens is null); n outside [0, max_len] counts as 0. With
+  // chunk == 0 every row merges all num_splits partials.
+  const int* seq_lens = nullptr;
+  int Hq = 1, len = 0, max_len = 0, chunk = 0;
 };
+
+// Keys per decode chunk: ceil(L / S) for a contiguous cache; for a paged
+// cache one length for all requests, the table's capacity over S rounded up
+// to whole 32-key stages, so request b uses ceil(n_b / chunk) <= S chunks.
+inline int decode_chunk(const DecodeArgs& a) {
+  if (a.block_table == nullptr) return (a.L + a.num_splits - 1) / a.num_splits;
+  const long long cap = 1LL * a.max_pages * a.page_size;
+  const long long c = (cap + a.num_splits - 1) / a.num_splits;
+  return int((c + 31) / 32 * 32);
+}
+
+// The merge that completes a decode call.
+inline MergeArgs decode_merge_args(const DecodeArgs& a) {
+  MergeArgs m{a.o_part, a.m_part, a.l_part, a.o, a.lse, a.B * a.Hq, a.num_splits, a.d,
+              ATTN_BF16, a.stream};
+  m.seq_lens = a.seq_lens;
+  m.Hq = a.Hq;
+  m.len = a.L;
+  m.max_len = a.block_table != nullptr ? a.max_pages * a.page_size : a.L;
+  m.chunk = decode_chunk(a);
+  return m;
+}
 
 // Workspace carving (bytes, 256-aligned sections).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
