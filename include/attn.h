@@ -102,9 +102,14 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, 
  * "Backpropagating Through Softmax": dS = P ∘ (dP - D) with dP = dO Vᵀ and the
  * row term D = rowsum(P ∘ dP), which equals rowsum(dO ∘ O) and is computed
  * that way by a preprocess kernel. Then dV = Pᵀ dO, dK = scale·dSᵀ Q and
- * dQ = scale·dS K; dQ is accumulated in float32 (the attention-residuals lab
- * reduces multi-writer gradients through float32 atomics) and converted at
- * the end. With GQA, dK and dV of a KV head sum over its query heads.
+ * dQ = scale·dS K. For dt = ATTN_BF16 with d = 128, dK and dV come from a
+ * pass over key tiles and dQ from a second pass over query tiles that
+ * recomputes S and dP, keeps dQ in tensor memory and writes it once in bf16
+ * (each gradient has one writer; the dQ accumulator in the workspace is not
+ * used). Otherwise dQ is accumulated across key tiles in float32 in the
+ * workspace (the attention-residuals lab reduces multi-writer gradients
+ * through float32 atomics) and converted at the end. With GQA, dK and dV of
+ * a KV head sum over its query heads.
  *
  * Inputs: q, k, v, o (forward output), dO, lse (forward LSE), all in `dt`
  * except lse (float32). Outputs dq, dk, dv in `dt`, overwritten.
