@@ -119,10 +119,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __shared__ DqBars bars;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Head-major order, the heaviest (latest, for causal) query tile of each
-  // head first; a head's K/V stay in L2 while its query tiles run.
-  const int bh = int(blockIdx.x) / n_qt;
-  const int qt = n_qt - 1 - int(blockIdx.x) % n_qt;
+  // Causal: query tiles in descending order across all heads, so the tiles
+  // with the most key steps start first and the last wave is made of the
+  // shortest ones (the K/V of the heads in flight together, 2 MB per head at
+  // N = 4096 and d = 128, fit in L2). Otherwise every tile has the same work:
+  // head-major order, a head's K/V staying in L2 while its tiles run.
+  const int n_bh = int(gridDim.x) / n_qt;
+  const int bh = causal ? int(blockIdx.x) % n_bh : int(blockIdx.x) / n_qt;
+  const int qt = n_qt - 1 - (causal ? int(blockIdx.x) / n_bh : int(blockIdx.x) % n_qt);
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int row0 = qt * kBM;

@@ -64,8 +64,17 @@ struct BwdCfg {
   static constexpr int kOffV = kOffK + kKVTile;
   static constexpr int kOffQ = kOffV + kKVTile;                      // [stage] Q, dO
   static constexpr int kOffP = kOffQ + kQStages * 2 * kQTile;       // [buf] dSᵀ
-  static constexpr int kOffVec = kOffP + kPsBufs * kPsTile;         // [stage] -LSE·log2e, -D
-  static constexpr int kSmemBytes = kOffVec + kQStages * 2 * BQ * 4;
+  // d = 128: the per-query terms enter the scores through the tensor core
+  // (see bwd_issue_sdp): a ones tile A (128 x 16) and per stage a tile B
+  // (BQ x 32: the bf16 parts of -LSE/scale, then of -D), both K-major
+  // without swizzle. d = 64: the softmax reads -LSE·log2e and -D from
+  // per-stage float vectors.
+  static constexpr bool kAugTerms = !kFusedDq;
+  static constexpr int kAugTile = BQ * 32 * 2;                      // B: 4 core-matrix columns
+  static constexpr int kOffOnes = kOffP + kPsBufs * kPsTile;        // A: 128 x 16 ones
+  static constexpr int kOffAug = kOffOnes + (kAugTerms ? kBK * 16 * 2 : 0);   // [stage] B
+  static constexpr int kOffVec = kOffAug + (kAugTerms ? kQStages * kAugTile : 0);
+  static constexpr int kSmemBytes = kOffVec + (kAugTerms ? 0 : kQStages * 2 * BQ * 4);
   static constexpr int kDynSmem = kSmemBytes + 1024;
   // tensor memory columns. d = 128: two (Sᵀ, dPᵀ) buffers of 64 + 64
   // columns, dV, dK 128 each (2·128 + 2·128 = 512). d = 64: one (Sᵀ, dPᵀ)
@@ -150,6 +159,19 @@ ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* do
     tc::mma_ss_warp(tmem + C::col_s(b), k_km + ka, qd + qb, idesc_sdp, kk > 0);
     tc::mma_ss_warp(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
   }
+  if (C::kAugTerms) {
+    // Sᵀ += 1 · (-LSE/scale parts), dPᵀ += 1 · (-D parts): one K = 16 step
+    // each, so Pᵀ = exp2(Sᵀ·scale·log2e) and dSᵀ = Pᵀ ∘ dPᵀ need no
+    // per-column loads. Layout: core matrices of 8 rows x 16 bytes; A has
+    // 2 along K (lbo 128) and 8-row groups every 256 bytes; B has 4 along K
+    // (lbo 128: -LSE parts in the first two, -D parts in the last two) and
+    // 8-row groups every 512 bytes.
+    const uint64_t ones = tc::smem_desc(smem_u32(smem + C::kOffOnes), 128, 256, tc::kLayoutNone);
+    const uint64_t aug = tc::smem_desc(smem_u32(smem + C::kOffAug + st * C::kAugTile), 128, 512,
+                                       tc::kLayoutNone);
+    tc::mma_ss_warp(tmem + C::col_s(b), ones, aug, idesc_sdp, 1u);
+    tc::mma_ss_warp(tmem + C::col_dp(b), ones, aug + (256 >> 4), idesc_sdp, 1u);
+  }
   tc::mma_commit_warp(done);
 }
 
@@ -228,6 +250,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   if (warp == 1) {
     tc::tmem_alloc(&bars.tmem_base, 512);
     tc::tmem_relinquish();
+  }
+  if (C::kAugTerms) {
+    // the ones tile (bf16 1.0 everywhere) and all-zero per-query tiles; the
+    // loader later rewrites only the parts' 16-byte chunks
+    uint32_t* ones = reinterpret_cast<uint32_t*>(smem + C::kOffOnes);
+    for (int i = tid; i < kBK * 16 / 2; i += kThreads) ones[i] = 0x3F803F80u;
+    uint32_t* aug = reinterpret_cast<uint32_t*>(smem + C::kOffAug);
+    for (int i = tid; i < C::kQStages * C::kAugTile / 4; i += kThreads) aug[i] = 0u;
+    fence_proxy_async_smem();   // read by the tensor core (async proxy)
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -308,11 +339,39 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.q_empty[st],
                                                        ((s / C::kQStages) - 1) & 1, abort_flag));
       if (!ok) break;
-      float* vec = reinterpret_cast<float*>(smem + C::kOffVec + st * 2 * BQ * 4);
+      if (C::kAugTerms) {
+        // query row n: 8-row group n/8 at 512 bytes, row n%8 at 16 bytes;
+        // chunk 0 = three bf16 parts of -LSE/scale (exact sum), chunk 2 =
+        // three parts of -D; chunks 1 and 3 stay zero
+        uint8_t* aug = smem + C::kOffAug + st * C::kAugTile;
+        const float inv_c = 1.f / (scale * kLog2e);
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        vec[u * 32 + lane] = nl[u];
-        vec[BQ + u * 32 + lane] = nd[u];
+        for (int u = 0; u < kPer; ++u) {
+          const int nrow = u * 32 + lane;
+          uint8_t* rowp = aug + (nrow >> 3) * 512 + (nrow & 7) * 16;
+          float vals[2] = {nl[u] * inv_c, nd[u]};
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const float v = vals[w];
+            const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
+            // -inf (a row past Nq): -inf, 0, 0 (P = 0 without a NaN)
+            const float r1 = isinf(v) ? 0.f : v - __bfloat162float(h1);
+            const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+            const __nv_bfloat16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+            const uint32_t w0 = uint32_t(__bfloat16_as_ushort(h1)) |
+                                (uint32_t(__bfloat16_as_ushort(h2)) << 16);
+            const uint32_t w1 = uint32_t(__bfloat16_as_ushort(h3));
+            *reinterpret_cast<uint4*>(rowp + w * 256) = make_uint4(w0, w1, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();   // read by the tensor core (async proxy)
+      } else {
+        float* vec = reinterpret_cast<float*>(smem + C::kOffVec + st * 2 * BQ * 4);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          vec[u * 32 + lane] = nl[u];
+          vec[BQ + u * 32 + lane] = nd[u];
+        }
       }
       mbar_arrive(&bars.q_full[st]);
       if (s + 1 < n) fetch(s + 1);
@@ -460,8 +519,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 #pragma unroll
           for (int h4 = 0; h4 < 2; ++h4) {
             const int cb = g8 * 8 + h4 * 4;         // column within the 32
-            const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + cb);       // -LSE·log2e
-            const float4 nd = *reinterpret_cast<const float4*>(vec + BQ + col0 + cb);  // -D
+            // -LSE·log2e and -D per column (d = 64); d = 128 has them in the scores
+            const float4 nl = C::kAugTerms ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                           : *reinterpret_cast<const float4*>(vec + col0 + cb);
+            const float4 nd = C::kAugTerms ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                           : *reinterpret_cast<const float4*>(vec + BQ + col0 + cb);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int e = cb + 2 * u;

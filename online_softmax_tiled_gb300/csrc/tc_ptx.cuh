@@ -105,6 +105,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 // offset >> 4; [46,48) version = 1; [49,52) base offset (0: tiles are
 // 1024-byte aligned); [61,64) layout (2 = 128-byte swizzle).
 constexpr uint32_t kLayoutSW128 = 2;
+// No swizzle: 8-row x 16-byte core matrices, each stored as 128 contiguous
+// bytes; for a K-major operand `lbo` is the byte step between core matrices
+// along K and `sbo` the step between 8-row groups.
+constexpr uint32_t kLayoutNone = 0;
 ATTN_DEVINL uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
   return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
          (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
