@@ -111,7 +111,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
               const float* __restrict__ row_term, int Hq, int Hkv, int Nq, int Nk, float scale,
-              int causal, int n_qt) {
+              int causal, int n_qt, int order_grp) {
   using C = DqCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -119,14 +119,12 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __shared__ DqBars bars;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Causal: query tiles in descending order across all heads, so the tiles
-  // with the most key steps start first and the last wave is made of the
-  // shortest ones (the K/V of the heads in flight together, 2 MB per head at
-  // N = 4096 and d = 128, fit in L2). Otherwise every tile has the same work:
-  // head-major order, a head's K/V staying in L2 while its tiles run.
-  const int n_bh = int(gridDim.x) / n_qt;
-  const int bh = causal ? int(blockIdx.x) % n_bh : int(blockIdx.x) / n_qt;
-  const int qt = n_qt - 1 - (causal ? int(blockIdx.x) / n_bh : int(blockIdx.x) % n_qt);
+  // Causal: heads in groups whose K/V fit in L2 together, and in a group the
+  // query tiles with the most key steps first, so each group (and the grid)
+  // ends with its shortest tiles. Otherwise head-major order.
+  int bh, rank;
+  grouped_tile_order(int(blockIdx.x), n_qt, int(gridDim.x) / n_qt, order_grp, bh, rank);
+  const int qt = n_qt - 1 - rank;
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int row0 = qt * kBM;
@@ -444,7 +442,8 @@ cudaError_t launch_bwd_dq(const BwdArgs& a) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, bwd_dq_kernel, mq, mk, mv, mdo, mdq, a.lse,
                             static_cast<const float*>(a.row_term), a.Hq, a.Hkv, a.Nq, a.Nk,
-                            a.scale, a.causal, n_qt);
+                            a.scale, a.causal, n_qt,
+                            order_group(a.causal != 0, 4LL * a.Nk * kD));
 }
 
 }  // namespace attn

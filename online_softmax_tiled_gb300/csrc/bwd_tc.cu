@@ -200,7 +200,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
               const float* __restrict__ lse, const float* __restrict__ row_term,
               float* __restrict__ dq_acc, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
-              int n_ktiles) {
+              int n_ktiles, int order_grp) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   // The dQ pass that follows (d = 128) reads none of this kernel's outputs:
@@ -212,11 +212,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __shared__ BwdBars bars;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Key tiles in ascending order across all heads: the tiles with the most
-  // query steps (causal) start first.
-  const int n_bhkv = int(gridDim.x) / n_ktiles;
-  const int ktile = int(blockIdx.x) / n_bhkv;
-  const int bhkv = int(blockIdx.x) % n_bhkv;
+  // Causal: KV heads in groups whose Q/dO fit in L2 together, and in a group
+  // the key tiles with the most query steps (the first ones) first.
+  // Otherwise head-major order.
+  int bhkv, ktile;
+  grouped_tile_order(int(blockIdx.x), n_ktiles, int(gridDim.x) / n_ktiles, order_grp, bhkv,
+                     ktile);
   const int b = bhkv / Hkv, g = bhkv % Hkv;
   const int group = Hq / Hkv;
   const int k0 = ktile * kBK;
@@ -674,13 +675,17 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   const int n_ktiles = (a.Nk + kBK - 1) / kBK;
+  // Q and dO of every query head of a KV head are re-read by all its key
+  // tiles; groups of up to 64 MiB of them (measured: one group of 32 heads
+  // of 2 MB ran 2 % faster than two groups of 16)
+  const int order_grp = order_group(a.causal != 0, 4LL * a.Nq * D * (a.Hq / a.Hkv), 64LL << 20);
   const long blocks = long(n_ktiles) * a.B * a.Hkv;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
   if (C::kFusedDq) {
     // d = 64 adds into the accumulator the preprocess zeroes: plain launch
     bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
         mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk,
-        a.scale, a.causal, n_ktiles);
+        a.scale, a.causal, n_ktiles, order_grp);
     return cudaGetLastError();
   }
   // d = 128: programmatic dependent of the preprocess; only the LSE/D loader
@@ -698,7 +703,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D>, mq, mk, mv, mdo, mdk, mdv, a.lse,
                             static_cast<const float*>(a.row_term), a.dq_acc, a.Hq, a.Hkv, a.Nq,
-                            a.Nk, a.scale, a.causal, n_ktiles);
+                            a.Nk, a.scale, a.causal, n_ktiles, order_grp);
 }
 
 }  // namespace

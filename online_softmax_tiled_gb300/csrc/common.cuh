@@ -223,6 +223,22 @@ ATTN_DEVINL bool mbar_wait2_warp(uint64_t* b1, uint32_t p1, uint64_t* b2, uint32
 // Bulk (non-tensor) async copy global -> shared, completing on an mbarrier.
 // Both addresses 16-byte aligned, size a multiple of 16.
 // ----------------------------------------------------------------------------
+// Order of the CTAs of a grid of n_tiles work tiles per head over n_heads
+// heads: heads in groups of `group` (the last group may be smaller), and
+// inside a group the tiles by rank, all heads of the group at rank 0, then
+// at rank 1, ... A kernel maps rank 0 to its heaviest tile, so that within
+// a group (sized on the host so that the group's re-read operands stay in
+// L2) the longest CTAs start first and the group ends with the shortest;
+// group = 1 is plain head-major order.
+ATTN_DEVINL void grouped_tile_order(int block, int n_tiles, int n_heads, int group, int& head,
+                                    int& rank) {
+  const int g0 = (block / (n_tiles * group)) * group;
+  const int hcount = min(group, n_heads - g0);
+  const int idx = block - g0 * n_tiles;
+  head = g0 + idx % hcount;
+  rank = idx / hcount;
+}
+
 ATTN_DEVINL void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

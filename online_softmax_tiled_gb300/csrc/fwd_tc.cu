@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
               float* __restrict__ lse, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
-              int n_qblk) {
+              int n_qblk, int order_grp) {
   using C = FwdCfg<D>;
   // d = 64: one MMA-issuing thread per query tile (each waits only on its own
   // tile). d = 128 (P̃ over the scores): one thread in the interleaved order
@@ -137,10 +137,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __shared__ Bars bars;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Head-major order (a head's K/V stay in L2 while its query blocks run),
-  // heaviest (latest, for causal) query block of each head first.
-  const int bh = int(blockIdx.x) / n_qblk;
-  const int qblk = n_qblk - 1 - int(blockIdx.x) % n_qblk;
+  // Heads in groups whose K/V fit in L2 together (causal; head-major
+  // otherwise); in a group the heaviest (latest) query blocks first.
+  int bh, rank;
+  grouped_tile_order(int(blockIdx.x), n_qblk, int(gridDim.x) / n_qblk, order_grp, bh, rank);
+  const int qblk = n_qblk - 1 - rank;
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int row0 = qblk * 2 * kBM;
@@ -601,7 +602,8 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D>, mq, mk, mv, mo, a.lse, a.Hq, a.Hkv, a.Nq,
-                            a.Nk, a.scale, a.causal, n_qblk);
+                            a.Nk, a.scale, a.causal, n_qblk,
+                            order_group(a.causal != 0, 4LL * a.Nk * D));
 }
 
 }  // namespace

@@ -103,6 +103,15 @@ inline MergeArgs decode_merge_args(const DecodeArgs& a) {
   return m;
 }
 
+// Heads per CTA-order group (grouped_tile_order): with a causal mask, as many
+// heads as keep `bytes_per_head` of re-read operands within `budget` bytes
+// of L2 (a quarter to a half of its 126 MB); otherwise 1 (head-major).
+inline int order_group(bool causal, long long bytes_per_head, long long budget = 32LL << 20) {
+  if (!causal || bytes_per_head <= 0) return 1;
+  const long long g = budget / bytes_per_head;
+  return g < 1 ? 1 : (g > (1 << 20) ? (1 << 20) : int(g));
+}
+
 // Workspace carving (bytes, 256-aligned sections).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
