@@ -25,6 +25,9 @@ from .attention import (  # noqa: F401
     softmax_jacobian,
     softmax_backward_jvp,
     attention_bwd,
+    mask_allowed,
+    attention_fwd_masked,
+    attention_bwd_masked,
     tiled_forward,
     decode_split_partials,
     merge_partials,

@@ -26,6 +26,10 @@ Sources, by page and section:
 * ML notes, prefill/decode and the KV cache: a serving cache is kept in
   fixed-size blocks reached through a per-request block table
   (``gather_paged``, ``decode_paged``).
+* Flash Attention 2 post, §Causal masking, "Why": option A handles
+  arbitrary masks (sliding window, document boundaries, prefix LM) as a
+  0 / -inf term added to the scores before the online softmax
+  (``mask_allowed``, ``attention_fwd_masked``, ``attention_bwd_masked``).
 
 Readings where the pages are silent (each also listed in the design notes):
 
@@ -39,6 +43,10 @@ Readings where the pages are silent (each also listed in the design notes):
 * GQA grouping is contiguous: query head h reads kv head h // (Hq // Hkv);
   dK and dV of a kv head sum over the query heads of its group.
 * Split s of L keys into S splits covers [s*c, min((s+1)*c, L)), c = ceil(L/S).
+* General masks: a window around each query's position on the key axis
+  (bottom-right aligned, as for causal), OR the first ``n_global`` keys,
+  AND, where given, a per-row key range [row_kv_start, row_kv_end) (the
+  row's document). Causal is the window (unbounded left, 0 right).
 
 Every function here is pinned by ``tests/test_oracle.py`` (worked example,
 closed forms, invariants, finite differences, brute force); none is
@@ -154,6 +162,89 @@ def attention_fwd_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray,
     rows = np.asarray(rows)
     s = scores(q[b, h, rows], k[b, g], scale, causal, nq_total=Nq, rows=rows)
     return softmax_rows(s) @ v[b, g], logsumexp_rows(s)
+
+
+# --------------------------------------------------------------------------
+# General masks (Flash Attention 2 post, §Causal masking, option A)
+# --------------------------------------------------------------------------
+
+def mask_allowed(nq: int, nk: int, window_left: int = -1, window_right: int = -1,
+                 n_global: int = 0, row_kv_start=None, row_kv_end=None) -> np.ndarray:
+    """Boolean visibility [nq, nk] of one batch entry.
+
+    Query row i sits at position i' = i + (nk - nq) of the key axis (the
+    bottom-right alignment of the causal case). Key j is visible iff it lies
+    in the row's window, i' - window_left <= j <= i' + window_right (a
+    negative bound is absent), or j < n_global; and, when row bounds are
+    given, row_kv_start[i] <= j < row_kv_end[i]. Causal is window (-1, 0);
+    a sliding window of W keys is (W - 1, 0); attention sinks add n_global;
+    prefix LM is causal with n_global = prefix length; documents packed in
+    one sequence give each row its document's key range.
+    """
+    i = np.arange(nq)[:, None] + (nk - nq)
+    j = np.arange(nk)[None, :]
+    win = np.ones((nq, nk), dtype=bool)
+    if window_left >= 0:
+        win &= j >= i - window_left
+    if window_right >= 0:
+        win &= j <= i + window_right
+    allowed = win | (j < n_global)
+    if row_kv_start is not None:
+        lo = np.asarray(row_kv_start)[:, None]
+        hi = np.asarray(row_kv_end)[:, None]
+        allowed &= (j >= lo) & (j < hi)
+    return allowed
+
+
+def _mask_of(mask, b: int, nq: int, nk: int) -> np.ndarray:
+    """mask_allowed for batch entry b of a mask given as a dict (None: all keys)."""
+    if mask is None:
+        return np.ones((nq, nk), dtype=bool)
+    rs, re = mask.get("row_kv_start"), mask.get("row_kv_end")
+    return mask_allowed(nq, nk, mask.get("window_left", -1), mask.get("window_right", -1),
+                        mask.get("n_global", 0), None if rs is None else rs[b],
+                        None if re is None else re[b])
+
+
+def attention_fwd_masked(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, mask):
+    """O and LSE under a general mask: S = scale · Q Kᵀ + M with M = 0 where a
+    key is visible and -inf elsewhere, then the plain softmax. A row with no
+    visible key has O = 0 and LSE = -inf."""
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    o = np.zeros((B, Hq, Nq, v.shape[-1]))
+    lse = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        allowed = _mask_of(mask, b, Nq, Nk)
+        for h in range(Hq):
+            g = _kv_head(h, Hq, Hkv)
+            s = np.where(allowed, scale * (q[b, h] @ k[b, g].T), NEG_INF)
+            o[b, h] = softmax_rows(s) @ v[b, g]
+            lse[b, h] = logsumexp_rows(s)
+    return o, lse
+
+
+def attention_bwd_masked(q: np.ndarray, k: np.ndarray, v: np.ndarray, do: np.ndarray,
+                         scale: float, mask):
+    """dQ, dK, dV under a general mask: P is zero on hidden keys, so the
+    softmax Jacobian-vector product dS = P ∘ (dP - rowsum(P ∘ dP)) is zero
+    there too; otherwise as ``attention_bwd``."""
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b in range(B):
+        allowed = _mask_of(mask, b, Nq, Nk)
+        for h in range(Hq):
+            g = _kv_head(h, Hq, Hkv)
+            p = softmax_rows(np.where(allowed, scale * (q[b, h] @ k[b, g].T), NEG_INF))
+            dp = do[b, h] @ v[b, g].T
+            ds = softmax_backward_jvp(p, dp)
+            dv[b, g] += p.T @ do[b, h]
+            dq[b, h] = scale * (ds @ k[b, g])
+            dk[b, g] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv
 
 
 # --------------------------------------------------------------------------

@@ -511,3 +511,214 @@ def test_paged_decode_closed_forms():
     np.testing.assert_allclose(o[2, 0], (w0 * vpages[0, 0, 0] + w1 * vpages[0, 0, 1]) / (w0 + w1),
                                rtol=1e-12)
     assert abs(lse[2, 0] - np.log(w0 + w1)) < 1e-12
+
+
+# -------------------------------------------------- general masks (option A)
+
+def _brute_masked(q, k, v, scale, visible):
+    """Pure-Python loops over one head: each row's softmax over the keys the
+    predicate visible(i, j) admits, built from index lists, not a mask matrix."""
+    nq, nk, dv = len(q), len(k), len(v[0])
+    out, lse = [], []
+    for i in range(nq):
+        s = [(j, scale * sum(q[i][t] * k[j][t] for t in range(len(q[i]))))
+             for j in range(nk) if visible(i, j)]
+        if not s:
+            out.append([0.0] * dv)
+            lse.append(-math.inf)
+            continue
+        mx = max(x for _, x in s)
+        z = sum(math.exp(x - mx) for _, x in s)
+        out.append([sum(math.exp(x - mx) / z * v[j][c] for j, x in s) for c in range(dv)])
+        lse.append(mx + math.log(z))
+    return np.array(out), np.array(lse)
+
+
+def _mask_inputs(B=2, Hq=2, Hkv=1, nq=9, nk=9, d=4, seed=70):
+    return (_rand((B, Hq, nq, d), seed), _rand((B, Hkv, nk, d), seed + 1),
+            _rand((B, Hkv, nk, d), seed + 2), _rand((B, Hq, nq, d), seed + 3))
+
+
+@pytest.mark.parametrize("nq,nk", [(9, 9), (5, 11)])
+def test_mask_causal_and_full_specs_equal_the_pinned_paths(nq, nk):
+    """Window (-1, 0) is the causal mask and (-1, -1) no mask at all: the
+    general path reproduces the pinned causal / unmasked oracle exactly."""
+    q, k, v, do = _mask_inputs(nq=nq, nk=nk)
+    for spec, causal in (({"window_left": -1, "window_right": 0}, True),
+                         ({"window_left": -1, "window_right": -1}, False), (None, False)):
+        o_m, l_m = oracle.attention_fwd_masked(q, k, v, 0.7, spec)
+        o_c, l_c = oracle.attention_fwd(q, k, v, 0.7, causal)
+        assert np.array_equal(o_m, o_c) and np.array_equal(l_m, l_c)
+        for a, b in zip(oracle.attention_bwd_masked(q, k, v, do, 0.7, spec),
+                        oracle.attention_bwd(q, k, v, do, 0.7, causal)):
+            np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("wl,wr,ng,nq,nk", [(2, 0, 0, 8, 8), (3, 0, 2, 8, 10), (1, 2, 0, 7, 7),
+                                            (-1, 1, 0, 6, 6), (2, -1, 3, 6, 9), (0, 0, 0, 5, 5)])
+def test_window_and_global_keys_brute_force(wl, wr, ng, nq, nk):
+    """Sliding windows, attention sinks (global keys), windows reaching right
+    of the diagonal: the matrix-built mask agrees with per-row index lists."""
+    q, k, v, _ = _mask_inputs(B=1, Hq=1, nq=nq, nk=nk, seed=80 + wl + 3 * wr + ng)
+    spec = {"window_left": wl, "window_right": wr, "n_global": ng}
+    o, lse = oracle.attention_fwd_masked(q, k, v, 0.9, spec)
+
+    def visible(i, j):
+        ip = i + nk - nq
+        in_win = (wl < 0 or j >= ip - wl) and (wr < 0 or j <= ip + wr)
+        return in_win or j < ng
+    ob, lb = _brute_masked(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), 0.9, visible)
+    np.testing.assert_allclose(o[0, 0], ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], lb, rtol=0, atol=1e-12)
+
+
+def _doc_bounds(lengths):
+    """Per-row key range [start, end) of each row's document, for documents of
+    the given lengths packed back to back (self-attention, nq = nk)."""
+    starts, ends, s = [], [], 0
+    for n in lengths:
+        starts += [s] * n
+        ends += [s + n] * n
+        s += n
+    return np.array(starts), np.array(ends)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_document_mask_is_attention_per_document(causal):
+    """Packed documents: the masked result equals plain (causal) attention run
+    on each document's slice alone."""
+    lengths = [4, 1, 6, 3]
+    n = sum(lengths)
+    q, k, v, do = _mask_inputs(B=1, Hq=2, Hkv=1, nq=n, nk=n, seed=90 + int(causal))
+    st, en = _doc_bounds(lengths)
+    spec = {"window_left": -1, "window_right": 0 if causal else -1,
+            "row_kv_start": st[None], "row_kv_end": en[None]}
+    o, lse = oracle.attention_fwd_masked(q, k, v, 0.8, spec)
+    grads = oracle.attention_bwd_masked(q, k, v, do, 0.8, spec)
+    s = 0
+    for ln in lengths:
+        sl = slice(s, s + ln)
+        o_d, l_d = oracle.attention_fwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], 0.8, causal)
+        np.testing.assert_allclose(o[:, :, sl], o_d, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[:, :, sl], l_d, rtol=0, atol=1e-13)
+        g_d = oracle.attention_bwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], do[:, :, sl], 0.8, causal)
+        for a, b in zip(grads, g_d):
+            np.testing.assert_allclose(a[:, :, sl], b, rtol=0, atol=1e-13)
+        s += ln
+
+
+def test_prefix_lm():
+    """Causal with the first P keys global: rows inside the prefix attend to
+    the whole prefix and nothing else; rows after it are ordinary causal rows."""
+    n, P = 10, 4
+    q, k, v, _ = _mask_inputs(B=1, Hq=1, nq=n, nk=n, seed=95)
+    o, lse = oracle.attention_fwd_masked(q, k, v, 0.6,
+                                         {"window_left": -1, "window_right": 0, "n_global": P})
+    o_p, l_p = oracle.attention_fwd(q[:, :, :P], k[:, :, :P], v[:, :, :P], 0.6, False)
+    o_c, l_c = oracle.attention_fwd(q, k, v, 0.6, True)
+    np.testing.assert_allclose(o[:, :, :P], o_p, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[:, :, :P], l_p, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(o[:, :, P:], o_c[:, :, P:], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse[:, :, P:], l_c[:, :, P:], rtol=0, atol=1e-13)
+
+
+def test_mask_rows_without_keys():
+    """Rows whose key range is empty (or whose window lies past the keys) get
+    O = 0, LSE = -inf and zero gradients; the other rows are unaffected."""
+    q, k, v, do = _mask_inputs(B=1, Hq=1, nq=6, nk=6, seed=97)
+    st = np.array([[0, 2, 3, 3, 0, 5]])
+    en = np.array([[3, 2, 6, 3, 6, 6]])            # rows 1 and 3 empty
+    spec = {"row_kv_start": st, "row_kv_end": en}
+    o, lse = oracle.attention_fwd_masked(q, k, v, 0.7, spec)
+    dq, dk, dv = oracle.attention_bwd_masked(q, k, v, do, 0.7, spec)
+    for r in (1, 3):
+        assert np.all(o[0, 0, r] == 0) and lse[0, 0, r] == -np.inf and np.all(dq[0, 0, r] == 0)
+    ob, lb = _brute_masked(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), 0.7,
+                           lambda i, j: st[0, i] <= j < en[0, i])
+    np.testing.assert_allclose(o[0, 0], ob, rtol=0, atol=1e-12)
+    assert np.array_equal(np.isinf(lse[0, 0]), np.isinf(lb))
+    # a window entirely to the left of the keys: nothing visible anywhere
+    o2, l2 = oracle.attention_fwd_masked(q, k, v, 0.7, {"window_left": 0, "window_right": 0,
+                                                       "row_kv_start": st, "row_kv_end": st})
+    assert np.all(o2 == 0) and np.all(l2 == -np.inf)
+
+
+def _masked_fd_error(spec, n=6, hq=2, hkv=1, d=3, seed=99, h=1e-6):
+    q, k, v, g = _mask_inputs(B=1, Hq=hq, Hkv=hkv, nq=n, nk=n, d=d, seed=seed)
+    an = oracle.attention_bwd_masked(q, k, v, g, 0.6, spec)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention_fwd_masked(q_, k_, v_, 0.6, spec)
+        return float((g * o).sum())
+    err = 0.0
+    for which, x in enumerate((q, k, v)):
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xs = [q.copy(), k.copy(), v.copy()]
+            xs[which][idx] += h
+            lp = loss(*xs)
+            xs[which][idx] -= 2 * h
+            lm = loss(*xs)
+            err = max(err, abs((lp - lm) / (2 * h) - an[which][idx]))
+    return err
+
+
+@pytest.mark.parametrize("spec", [
+    {"window_left": 1, "window_right": 0, "n_global": 1},
+    {"window_left": -1, "window_right": 1},
+    {"window_left": -1, "window_right": 0,
+     "row_kv_start": np.array([[0, 0, 2, 2, 2, 5]]), "row_kv_end": np.array([[2, 2, 5, 5, 5, 6]])},
+])
+def test_masked_bwd_finite_differences(spec):
+    assert _masked_fd_error(spec) < 1e-7
+
+
+def test_planted_mask_mistakes_are_caught(monkeypatch):
+    """Plausible slips in the mask builder: each makes a mask pin fail."""
+    def window_error():
+        nq, nk, wl, wr, ng = 6, 9, 2, 0, 2
+        q, k, v, _ = _mask_inputs(B=1, Hq=1, nq=nq, nk=nk, seed=101)
+        o, _ = oracle.attention_fwd_masked(q, k, v, 0.9, {"window_left": wl, "window_right": wr,
+                                                          "n_global": ng})
+
+        def visible(i, j):
+            ip = i + nk - nq
+            return (ip - wl <= j <= ip + wr) or j < ng
+        ob, _ = _brute_masked(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), 0.9, visible)
+        return np.max(np.abs(o[0, 0] - ob))
+
+    def document_error():
+        lengths = [3, 4, 2]
+        q, k, v, _ = _mask_inputs(B=1, Hq=1, nq=9, nk=9, seed=102)
+        st, en = _doc_bounds(lengths)
+        o, _ = oracle.attention_fwd_masked(q, k, v, 0.8, {"row_kv_start": st[None],
+                                                          "row_kv_end": en[None]})
+        o_d = [oracle.attention_fwd(q[:, :, a:b], k[:, :, a:b], v[:, :, a:b], 0.8)[0]
+               for a, b in ((0, 3), (3, 7), (7, 9))]
+        return np.max(np.abs(o - np.concatenate(o_d, axis=2)))
+
+    checks = [window_error, document_error]
+    assert max(c() for c in checks) < 1e-9
+    orig = oa.mask_allowed
+    mutants = {
+        "window one key wider": lambda nq, nk, wl=-1, wr=-1, ng=0, rs=None, re=None:
+            orig(nq, nk, wl + 1 if wl >= 0 else wl, wr, ng, rs, re),
+        "global keys dropped": lambda nq, nk, wl=-1, wr=-1, ng=0, rs=None, re=None:
+            orig(nq, nk, wl, wr, 0, rs, re),
+        "top-left alignment": lambda nq, nk, wl=-1, wr=-1, ng=0, rs=None, re=None:
+            orig(nq, nq, wl, wr, ng, rs, re)[:, :nk] if nk <= nq else
+            np.pad(orig(nq, nq, wl, wr, ng, rs, re), ((0, 0), (0, nk - nq))),
+        "document end inclusive": lambda nq, nk, wl=-1, wr=-1, ng=0, rs=None, re=None:
+            orig(nq, nk, wl, wr, ng, rs, None if re is None else np.asarray(re) + 1),
+    }
+    for name, fn in mutants.items():
+        with monkeypatch.context() as mp:
+            mp.setattr(oa, "mask_allowed", fn)
+            errs = []
+            for c in checks:
+                try:
+                    errs.append(c())
+                except Exception:
+                    errs.append(np.inf)
+            assert max(errs) > 1e-6, f"pins missed the planted mistake: {name}"
