@@ -18,6 +18,7 @@ over ranks of the timed region ("scaling": "weak").
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -36,8 +37,41 @@ L2_BYTES = 129 << 20
 # ----------------------------------------------------------------- workload math
 
 def make_workload_inputs(w):
-    from workloads import make_inputs, make_paged_inputs
-    return make_paged_inputs(w) if w.kind == "decode_paged" else make_inputs(w)
+    from workloads import make_doc_bounds, make_inputs, make_paged_inputs
+    if w.kind == "decode_paged":
+        return make_paged_inputs(w)
+    x = make_inputs(w)
+    if w.doc_mean > 0:
+        x["row_kv_start"], x["row_kv_end"] = make_doc_bounds(w.B, w.Nq, w.doc_mean, w.seed + 1)
+    return x
+
+
+def mask_spec(w, x):
+    """The workload's mask as the oracle's dict (host arrays)."""
+    spec = {"window_left": w.window_left, "window_right": w.window_right, "n_global": w.n_global}
+    if "row_kv_start" in x:
+        spec["row_kv_start"] = x["row_kv_start"].numpy()
+        spec["row_kv_end"] = x["row_kv_end"].numpy()
+    return spec
+
+
+def visible_pairs(w, x):
+    """Visible (query, key) pairs of one head, summed over the batch: each
+    row sees [lo1, hi1] (window within its key range) and [lo2, hi2] (global
+    keys within it)."""
+    import numpy as np
+    i = np.arange(w.Nq, dtype=np.int64)[None, :] + (w.Nk - w.Nq)
+    s = np.zeros((w.B, w.Nq), dtype=np.int64)
+    e = np.full((w.B, w.Nq), w.Nk, dtype=np.int64)
+    if "row_kv_start" in x:
+        s, e = x["row_kv_start"].numpy().astype(np.int64), x["row_kv_end"].numpy().astype(np.int64)
+    lo1 = np.maximum(i - w.window_left if w.window_left >= 0 else 0, s)
+    hi1 = np.minimum(i + w.window_right if w.window_right >= 0 else w.Nk - 1, e - 1)
+    lo2, hi2 = s, np.minimum(w.n_global, e) - 1
+    n1 = np.maximum(0, hi1 - lo1 + 1)
+    n2 = np.maximum(0, hi2 - lo2 + 1)
+    ov = np.maximum(0, np.minimum(hi1, hi2) - np.maximum(lo1, lo2) + 1)
+    return int((n1 + n2 - ov).sum())
 
 
 def paged_bytes(w, seq_lens):
@@ -62,6 +96,8 @@ def algorithmic_units(w, inputs=None):
     if w.kind == "decode":
         bytes_ = 2 * w.B * w.Hkv * w.Nk * w.d * 2 + 2 * w.B * w.Hq * w.d * 2
         return bytes_, "GB/s", "hbm"
+    if w.masked:
+        return 4.0 * w.Hq * w.d * visible_pairs(w, inputs), "TFLOP/s", "tensor"
     if w.causal:
         shift = w.Nk - w.Nq
         pairs = sum(min(w.Nk, i + shift + 1) for i in range(w.Nq))
@@ -195,17 +231,30 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
     heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
     per_head = units_total / len(heads)
     r = w.Hq // w.Hkv
+    done_units = 0.0
     for b, h in heads:
         sl = lambda t, hh: to_f64(t[b:b + 1, hh:hh + 1])
         q, k, v = sl(inputs["q"], h), sl(inputs["k"], h // r), sl(inputs["v"], h // r)
         if w.kind == "bwd":
             oracle.attention_bwd(q, k, v, sl(inputs["do"], h), w.scale, w.causal)
+            done_units += per_head
+        elif w.masked:
+            spec = mask_spec(w, inputs)
+            xb = {}
+            for key in ("row_kv_start", "row_kv_end"):
+                if key in spec:
+                    spec[key] = spec[key][b:b + 1]
+                    xb[key] = inputs[key][b:b + 1]
+            oracle.attention_fwd_masked(q, k, v, w.scale, spec)
+            done_units += 4.0 * w.d * visible_pairs(
+                dataclasses.replace(w, B=1), xb) if xb else units_total / len(heads)
         else:
             oracle.attention_fwd(q, k, v, w.scale, w.causal)
+            done_units += per_head
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    return per_head * done, time.perf_counter() - t0, f"{done} of {len(heads)} heads (b, h)"
+    return done_units, time.perf_counter() - t0, f"{done} of {len(heads)} heads (b, h)"
 
 
 def input_bytes(inputs):
@@ -259,6 +308,12 @@ def workload_config(w, flushed: bool):
            "d": w.d, "causal": w.causal, "dtype": w.dtype}
     if w.kind in ("decode", "decode_paged"):
         cfg["num_splits"] = w.num_splits
+    if w.masked:
+        cfg["mask"] = {"window_left": w.window_left, "window_right": w.window_right,
+                       "n_global": w.n_global}
+        if w.doc_mean:
+            cfg["mask"]["documents"] = (f"packed, lengths uniform on [1, {2 * w.doc_mean - 1}], "
+                                        "row key range = the row's document")
     if w.kind == "decode_paged":
         cfg["Nk"] = f"per-request lengths uniform on [1, {2 * w.Nk - 1}] (mean {w.Nk})"
         cfg["page_size"] = w.page_size
@@ -347,7 +402,15 @@ def run_gpu(args, w):
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
     # --- one step of the hot path, device-resident inputs
-    if w.kind == "fwd":
+    if w.kind == "fwd" and w.masked:
+        o = torch.empty_like(x["q"])
+        lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
+        amask = ost.make_mask(w.window_left, w.window_right, w.n_global, x.get("row_kv_start"),
+                              x.get("row_kv_end"))
+        step = lambda: ost.attn_fwd_masked(x["q"], x["k"], x["v"], o, lse, w.scale, amask, stream)
+        launches_per_step = 1
+        outs = (o, lse)
+    elif w.kind == "fwd":
         o = torch.empty_like(x["q"])
         lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
         step = lambda: ost.attn_fwd(x["q"], x["k"], x["v"], o, lse, w.scale, w.causal, stream)

@@ -73,7 +73,8 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  * (the attention-residuals kernel lab on manishklach.github.io saves the row
  * max and denominator for the backward; LSE = max + ln(denominator) carries
  * both). Scores are scaled by `scale` (1/sqrt(d) in the ML notes'
- * attention Q&A on haolingpu.github.io).
+ * attention Q&A on haolingpu.github.io); scale must be positive and finite
+ * (the kernels take each row maximum before scaling).
  *
  * q [B,Hq,Nq,d], k/v [B,Hkv,Nk,d] in `dt`; o [B,Hq,Nq,d] written in `dt`;
  * lse [B,Hq,Nq] float32 written (may be NULL to skip it).
@@ -85,6 +86,49 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
 ATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                      attn_dtype dt, void* stream);
+
+/*
+ * Attention mask.
+ *
+ * Flash Attention 2 post, section "Causal masking", option A and its "Why":
+ * any mask (sliding window, document boundaries, prefix LM, ...) is a
+ * 0 / -inf term added to the scores before the online softmax; key tiles no
+ * query row of a tile can see are skipped, tiles that straddle a boundary
+ * are masked element by element.
+ *
+ * Query row i (0-based) sits at position i' = i + (Nk - Nq) of the key axis
+ * (bottom-right alignment, as for causal). Key j is visible to row i of
+ * batch entry b iff
+ *     [ (window_left  < 0 || j >= i' - window_left)  and
+ *       (window_right < 0 || j <= i' + window_right) ]   (its window)
+ *     or j < n_global                                    (global keys)
+ *   and, when row_kv_start / row_kv_end are given,
+ *     row_kv_start[b*Nq + i] <= j < row_kv_end[b*Nq + i] (its key range).
+ * Examples: no mask {-1, -1, 0}; causal {-1, 0, 0}; sliding window of W keys
+ * {W-1, 0, 0}; attention sinks plus a window {W-1, 0, n_sink}; prefix LM
+ * with a prefix of P tokens {-1, 0, P}; documents packed into one sequence:
+ * each row's document as its key range, with {-1, 0, 0} (causal within a
+ * document) or {-1, -1, 0}.
+ * row_kv_start and row_kv_end: [B, Nq] int32 in device memory, both or
+ * neither; values are clipped to [0, Nk]; the same for every head.
+ * A row with no visible key gets O = 0, LSE = -inf.
+ */
+typedef struct {
+  int window_left;
+  int window_right;
+  int n_global;
+  const int* row_kv_start;
+  const int* row_kv_end;
+} attn_mask;
+
+/*
+ * attn_fwd under a general mask (see attn_mask). mask == NULL: no mask.
+ * Any Nq, Nk > 0 (rows may have no visible key); otherwise as attn_fwd.
+ */
+ATTN_API attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                     float scale, const attn_mask* mask, attn_dtype dt,
+                                     void* stream);
 
 /*
  * Bytes of device scratch attn_bwd needs: the row term D [B,Hq,Nq] float32

@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     ATTN_F32,
     ATTN_OK,
     AttnError,
+    AttnMask,
     attn_bwd,
     attn_bwd_workspace_size,
     attn_decode_paged,
@@ -18,6 +19,7 @@ from ._binding import (  # noqa: F401
     attn_decode_splitkv_noalloc,
     attn_decode_workspace_size,
     attn_fwd,
+    attn_fwd_masked,
     attn_merge_partials,
     attn_status_string,
     attn_sync_status,
@@ -26,5 +28,6 @@ from ._binding import (  # noqa: F401
     decode_paged,
     forward,
     lib,
+    make_mask,
 )
 from ._build import LIB_PATH, build  # noqa: F401

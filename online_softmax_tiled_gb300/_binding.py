@@ -35,9 +35,19 @@ class AttnError(RuntimeError):
 
 _LIB = None
 
+
+class AttnMask(ctypes.Structure):
+    """The C ``attn_mask``: window (left, right; -1 = unbounded), n_global
+    keys visible to every row, optional per-row key ranges [B, Nq] int32."""
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("n_global", ctypes.c_int), ("row_kv_start", ctypes.c_void_p),
+                ("row_kv_end", ctypes.c_void_p)]
+
 _SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_masked": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
+                        [ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 6),
     "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 +
                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
@@ -121,6 +131,29 @@ def attn_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                         float(scale), int(bool(causal)), _dt(q), _stream(stream))
     _check(st, "attn_fwd")
+
+
+def make_mask(window_left=-1, window_right=-1, n_global=0, row_kv_start=None,
+              row_kv_end=None) -> AttnMask:
+    """An ``attn_mask``; the row ranges are int32 device tensors [B, Nq]
+    kept alive by the caller for as long as the call runs."""
+    for t in (row_kv_start, row_kv_end):
+        if t is not None and (t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("row ranges must be contiguous int32 device tensors")
+    return AttnMask(int(window_left), int(window_right), int(n_global),
+                    None if row_kv_start is None else row_kv_start.data_ptr(),
+                    None if row_kv_end is None else row_kv_end.data_ptr())
+
+
+def attn_fwd_masked(q, k, v, o, lse, scale: float, mask, stream=None):
+    """attn_fwd under an ``attn_mask`` (``make_mask``; None: no mask)."""
+    _device_contig(q, k, v, o, lse)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    m = None if mask is None else ctypes.byref(mask)
+    st = lib().attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq,
+                               Nk, d, float(scale), m, _dt(q), _stream(stream))
+    _check(st, "attn_fwd_masked")
 
 
 def attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d) -> int:
@@ -207,13 +240,17 @@ def attn_sync_status(stream=None) -> int:
 # ------------------------------------------- allocating conveniences (torch)
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, with_lse: bool = True,
-            stream=None):
-    """O, LSE = attention(q, k, v); outputs allocated by torch on q's device."""
+            stream=None, mask: AttnMask | None = None):
+    """O, LSE = attention(q, k, v); outputs allocated by torch on q's device.
+    ``mask`` (``make_mask``) replaces ``causal`` when given."""
     d = q.shape[-1]
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if with_lse else None
-    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    if mask is not None:
+        attn_fwd_masked(q, k, v, o, lse, scale, mask, stream)
+    else:
+        attn_fwd(q, k, v, o, lse, scale, causal, stream)
     return o, lse
 
 

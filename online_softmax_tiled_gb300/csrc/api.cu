@@ -73,20 +73,68 @@ const char* attn_status_string(attn_status s) {
   return "unknown status";
 }
 
+namespace {
+
+inline bool scale_ok(float scale) { return scale > 0.f && scale <= 3.4e38f; }   // rejects NaN too
+
+MaskSpec mask_spec(const attn_mask* m) {
+  MaskSpec ms;
+  if (m != nullptr) {
+    ms.window_left = m->window_left < 0 ? -1 : m->window_left;
+    ms.window_right = m->window_right < 0 ? -1 : m->window_right;
+    ms.n_global = m->n_global < 0 ? 0 : m->n_global;
+    ms.row_kv_start = m->row_kv_start;
+    ms.row_kv_end = m->row_kv_end;
+  }
+  return ms;
+}
+
+attn_status check_mask(const attn_mask* m) {
+  if (m == nullptr) return ATTN_OK;
+  if ((m->row_kv_start == nullptr) != (m->row_kv_end == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(m->row_kv_start) & 3u) ||
+      (reinterpret_cast<uintptr_t>(m->row_kv_end) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, float scale, const MaskSpec& ms,
+                       attn_dtype dt, void* stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && !aligned16(lse)))
+    return ATTN_ERR_MISALIGNED;
+  const int causal = (ms.window_left < 0 && ms.window_right == 0 && ms.n_global == 0 &&
+                      ms.row_kv_start == nullptr) ? 1 : 0;
+  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, dt,
+            static_cast<cudaStream_t>(stream)};
+  a.mask = ms;
+  if (dt == ATTN_BF16) return from_cuda(launch_fwd_tc(a));
+  return from_cuda(launch_fwd_simt(a));
+}
+
+}  // namespace
+
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                      attn_dtype dt, void* stream) {
   attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, causal, dt);
   if (st != ATTN_OK) return st;
-  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
-  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;  // NaN scale
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-      (lse && !aligned16(lse)))
-    return ATTN_ERR_MISALIGNED;
-  FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, dt,
-            static_cast<cudaStream_t>(stream)};
-  if (dt == ATTN_BF16) return from_cuda(launch_fwd_tc(a));
-  return from_cuda(launch_fwd_simt(a));
+  MaskSpec ms;
+  if (causal) ms.window_right = 0;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, ms, dt, stream);
+}
+
+attn_status attn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                            const attn_mask* mask, attn_dtype dt, void* stream) {
+  // any Nq, Nk: rows may see nothing, so the causal Nq <= Nk rule does not apply
+  attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, 0, dt);
+  if (st != ATTN_OK) return st;
+  if ((st = check_mask(mask)) != ATTN_OK) return st;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, mask_spec(mask), dt, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
@@ -103,7 +151,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, causal, dt);
   if (st != ATTN_OK) return st;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
-  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
   for (const void* p : ptrs)
     if (!aligned16(p)) return ATTN_ERR_MISALIGNED;

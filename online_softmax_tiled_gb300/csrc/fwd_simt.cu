@@ -9,9 +9,13 @@
 // by l once after the last tile. The probabilities of a tile are taken
 // relative to the new running max directly, P̃ = exp(S - m_new), which equals
 // the page's e^(m_ij - m_new)·exp(S - m_ij) with one exponential fewer.
+// Masks (the post's section "Causal masking", option A): the CTA visits only
+// the key tiles some of its rows see (mask.cuh) and masks the rest per
+// element.
 
 #include "common.cuh"
 #include "launchers.h"
+#include "mask.cuh"
 
 namespace attn {
 namespace {
@@ -34,7 +38,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 T* __restrict__ o, float* __restrict__ lse, int Hq, int Hkv, int Nq, int Nk,
-                float scale, int causal) {
+                float scale, MaskSpec mask) {
   extern __shared__ float smem[];
   float* sQ = smem;                         // [kBR][D+1]
   float* sK = sQ + kBR * (D + 1);           // [kBC][D+1]
@@ -68,11 +72,21 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     for (int c = 0; c < DC; ++c) acc[i][c] = 0.f;
   }
 
-  const int shift = Nk - Nq;  // bottom-right causal alignment
-  int kv_end = Nk;
-  if (causal) kv_end = min(Nk, max(0, row0 + kBR - 1 + shift + 1));
+  // Keys of this thread's four rows, and the key tiles any row of the CTA sees.
+  __shared__ PlanSlots slots;
+  if (tid == 0) slots.init();
+  __syncthreads();
+  RowKeys rk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    rk[i] = row_keys(mask, b, row0 + 4 * ty + i, Nq, Nk);
+    plan_add_rows(&slots, rk[i], 0);
+  }
+  __syncthreads();
+  const KeyTilePlan plan = make_plan(slots, kBC);
 
-  for (int kv0 = 0; kv0 < kv_end; kv0 += kBC) {
+  for (int jt = 0; jt < plan.total(); ++jt) {
+    const int kv0 = plan.tile(jt) * kBC;
     __syncthreads();
     for (int idx = tid; idx < kBC * D; idx += kThreads) {
       const int r = idx / D, c = idx % D;
@@ -104,12 +118,11 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     // Steps 2-4: masked row max, probabilities, running statistics
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row = row0 + 4 * ty + i;
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int col = kv0 + tx + 8 * c;
-        const bool vis = col < Nk && (!causal || col <= row + shift);
+        const bool vis = rk[i].visible(col);   // also false past Nk
         s[i][c] = vis ? s[i][c] * scale : -INFINITY;
         mx = fmaxf(mx, s[i][c]);
       }
@@ -175,7 +188,7 @@ cudaError_t launch_fwd_simt_t(const FwdArgs& a) {
   dim3 grid((a.Nq + kBR - 1) / kBR, a.B * a.Hq);
   fwd_simt_kernel<T, D><<<grid, kThreads, smem, a.stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
-      static_cast<T*>(a.o), a.lse, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.causal);
+      static_cast<T*>(a.o), a.lse, a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.mask);
   return cudaGetLastError();
 }
 

@@ -6,9 +6,10 @@
 // tile Q_i and each key/value tile K_j, V_j: S_ij = scale·Q_i K_jᵀ, running
 // row max m, P̃ = exp(S - m), running denominator l, Õ rescaled by
 // exp(m_old - m_new) and accumulated with P̃ V_j; after the last tile
-// O_i = Õ_i / l_i and LSE = m + ln l. Causal masking per the post's section
-// "Causal masking": tiles wholly in the future are skipped (option B loop
-// bounds) and the tiles that straddle the diagonal are masked (option A).
+// O_i = Õ_i / l_i and LSE = m + ln l. Masks per the post's section "Causal
+// masking", option A, which covers arbitrary masks: the CTA visits only the
+// key tiles some row of it can see (mask.cuh: at most two ranges) and the
+// tiles that straddle a row's boundary are masked element by element.
 //
 // GB300 mapping (differs from the post's SRAM-only picture):
 //  * One CTA owns two 128-row query tiles of one head (256 rows) and streams
@@ -31,6 +32,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "mask.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -75,6 +77,7 @@ struct Bars {
   uint64_t mma_drain[2];
   uint32_t tmem_base;
   int abort;
+  PlanSlots plan;   // keys the CTA's rows see (general masks)
 };
 
 ATTN_DEVINL void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
@@ -104,23 +107,25 @@ ATTN_DEVINL void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
       : "memory");
 }
 
-// Number of K/V tiles query tile `t` of this CTA must visit (0 if the tile
-// has no valid row).
-ATTN_DEVINL int kv_tiles_for(int row_first, int Nq, int Nk, int causal) {
+// Number of K/V tiles a query tile starting at row_first visits without a
+// general mask (0 if the tile has no valid row): all of them, or up to the
+// causal diagonal.
+ATTN_DEVINL int kv_tiles_for(int row_first, int Nq, int Nk, bool causal) {
   if (row_first >= Nq) return 0;
   const int nk_tiles = (Nk + kBN - 1) / kBN;
   if (!causal) return nk_tiles;
   const int row_last = min(row_first + kBM - 1, Nq - 1);
-  const int last_key = row_last + (Nk - Nq);            // bottom-right alignment
-  return min(nk_tiles, last_key / kBN + 1);
+  return min(nk_tiles, (row_last + (Nk - Nq)) / kBN + 1);   // bottom-right alignment
 }
 
-template <int D>
+// kGeneral = false: no mask or causal only (the CTA visits key tiles 0, 1, ...
+// and masks past a single per-row limit); true: any MaskSpec.
+template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
-              float* __restrict__ lse, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
-              int n_qblk, int order_grp) {
+              float* __restrict__ lse, int Hq, int Hkv, int Nq, int Nk, float scale,
+              MaskSpec mask, int n_qblk, int order_grp) {
   using C = FwdCfg<D>;
   // d = 64: one MMA-issuing thread per query tile (each waits only on its own
   // tile). d = 128 (P̃ over the scores): one thread in the interleaved order
@@ -135,6 +140,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ Bars bars;
+  __shared__ int4 keys_of_row[2 * kBM];   // each row's visible key intervals
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Heads in groups whose K/V fit in L2 together (causal; head-major
@@ -145,11 +151,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int row0 = qblk * 2 * kBM;
-  const int n_t[2] = {kv_tiles_for(row0, Nq, Nk, causal), kv_tiles_for(row0 + kBM, Nq, Nk, causal)};
-  const int nj = max(n_t[0], n_t[1]);
 
   if (tid == 0) {
     bars.abort = 0;
+    bars.plan.init();
     mbar_init(&bars.q_full, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
@@ -177,24 +182,61 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
-  // Register split: 128 x 80 (TMA, MMA, idle warps) + 256 x 208 (softmax)
-  // <= 384 x 168 registers the CTA is launched with.
+  // The Q tiles do not depend on the mask: their loads start first.
+  if (warp == 0 && lane == 0) {
+    pdl_wait_primary();
+    tc::tma_prefetch_desc(&map_q);
+    tc::tma_prefetch_desc(&map_k);
+    tc::tma_prefetch_desc(&map_v);
+    mbar_arrive_expect_tx(&bars.q_full, 2 * C::kTileBytes);
+    for (int t = 0; t < 2; ++t)
+      for (int a = 0; a < C::kAtoms; ++a)
+        tc::tma_load_3d(smem + C::kQOff + t * C::kTileBytes + a * (kBM * 128), &map_q, 64 * a,
+                        row0 + t * kBM, bh, &bars.q_full);
+  }
+  // The key tiles to visit. Without row ranges the plan follows from the
+  // mask directly (no barrier: the loads start at once); with them every
+  // softmax thread (one query row) adds the keys its row sees and all roles
+  // wait for the sum. Query tile t visits the prefix of the plan that ends
+  // with its last visible key.
+  PlanSlots slots;
+  if (!kGeneral) {
+    // tiles 0 .. n-1; the plan is only read by the general path
+    const bool causal = mask.window_right == 0;
+    slots.init();
+    slots.lo1 = 0;
+    slots.hi1 = Nk - 1;
+    slots.last[0] = kv_tiles_for(row0, Nq, Nk, causal) * kBN - 1;
+    slots.last[1] = kv_tiles_for(row0 + kBM, Nq, Nk, causal) * kBN - 1;
+  } else if (mask.row_kv_start == nullptr) {
+    slots = plan_slots_direct(mask, row0, kBM, 2, Nq, Nk);
+    if (tid == 0) bars.plan = slots;   // the producer thread reads it back below
+  } else {
+    if (warp >= 4) {
+      const int t = (warp - 4) / 4;
+      pdl_wait_primary();                                    // the ranges are inputs
+      const RowKeys rk = row_keys(mask, b, row0 + t * kBM + (warp % 4) * 32 + lane, Nq, Nk);
+      store_row_keys(&keys_of_row[tid - 128], rk);
+      plan_add_rows(&bars.plan, rk, t);
+    }
+    __syncthreads();
+    slots = bars.plan;
+  }
+  const KeyTilePlan plan = make_plan(slots, kBN);
+  const int n_t[2] = {slots.last[0] >= 0 ? plan.count_upto(slots.last[0] / kBN) : 0,
+                      slots.last[1] >= 0 ? plan.count_upto(slots.last[1] / kBN) : 0};
+  auto key_tile = [&](int j) {
+    return kGeneral ? make_plan_volatile(&bars.plan, kBN).tile(j) : j;
+  };
+  const int nj = max(n_t[0], n_t[1]);
+
   // Register split, set inside each role: 128 x 80 (TMA, MMA, idle warps) +
   // 256 x 208 (softmax) <= 384 x 168 registers the CTA is launched with.
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     regs_dec<80>();
-    pdl_wait_primary();
     if (lane == 0 && nj > 0) {
-      tc::tma_prefetch_desc(&map_q);
-      tc::tma_prefetch_desc(&map_k);
-      tc::tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(&bars.q_full, 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int a = 0; a < C::kAtoms; ++a)
-          tc::tma_load_3d(smem + C::kQOff + t * C::kTileBytes + a * (kBM * 128), &map_q, 64 * a,
-                          row0 + t * kBM, bh, &bars.q_full);
       int issued_k = 0, issued_v = 0;
       bool ok = true;
       for (int j = 0; j < nj && ok; ++j) {
@@ -205,14 +247,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         mbar_arrive_expect_tx(&bars.k_full[st], C::kTileBytes);
         for (int a = 0; a < C::kAtoms; ++a)
           tc::tma_load_3d(smem + C::kKOff + st * C::kTileBytes + a * (kBN * 128), &map_k, 64 * a,
-                          j * kBN, kvh, &bars.k_full[st]);
+                          key_tile(j) * kBN, kvh, &bars.k_full[st]);
         ++issued_k;
         if (j >= C::kStages) ok = mbar_wait_bounded(&bars.v_empty[st], ph ^ 1, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars.v_full[st], C::kTileBytes);
         for (int a = 0; a < C::kAtoms; ++a)
           tc::tma_load_3d(smem + C::kVOff + st * C::kTileBytes + a * (kBN * 128), &map_v, 64 * a,
-                          j * kBN, kvh, &bars.v_full[st]);
+                          key_tile(j) * kBN, kvh, &bars.v_full[st]);
         ++issued_v;
       }
       if (!ok) {
@@ -405,8 +447,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const uint32_t p_addr = tmem + lane_base + (t == 0 ? C::kColP0 : C::kColP1);
     const uint32_t o_addr = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
     const float c = scale * kLog2e;               // scores in log2 units
-    const int shift = Nk - Nq;
     const int nt = n_t[t];
+    // general mask: this row's key intervals; otherwise its last key
+    const RowKeys rk = !kGeneral ? RowKeys{1, 0, 1, 0}
+                       : mask.row_kv_start == nullptr ? row_keys(mask, b, row, Nq, Nk)
+                                                      : load_row_keys(&keys_of_row[tid - 128]);
+    const int limit = mask.window_right == 0 ? min(Nk - 1, row + (Nk - Nq)) : Nk - 1;
 
     float m_ref = -INFINITY;                       // reference max (log2 units)
     float l_run = 0.f;
@@ -430,10 +476,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         mbar_arrive(&bars.s_free[t]);
       }
 
-      // Mask keys past the end and, for causal, keys after this row's limit.
-      const int key0 = j * kBN;
-      const int limit = causal ? min(Nk - 1, row + shift) : Nk - 1;   // last visible key
-      if (key0 + kBN - 1 > limit) {
+      // Mask the keys this row does not see (past the end included) in a
+      // tile that straddles one of its bounds.
+      const int key0 = (kGeneral ? plan.tile(j) : j) * kBN;
+      if (kGeneral) {
+        if (!rk.covers(key0, key0 + kBN - 1)) {
+#pragma unroll
+          for (int w = 0; w < kBN / 32; ++w) {
+            const uint32_t vis = rk.bits(key0, w);
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              if (!(vis & (1u << cc))) s[32 * w + cc] = -INFINITY;
+          }
+        }
+      } else if (key0 + kBN - 1 > limit) {
 #pragma unroll
         for (int cc = 0; cc < kBN; ++cc)
           if (key0 + cc > limit) s[cc] = -INFINITY;
@@ -524,24 +580,31 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       mbar_arrive(&bars.p_full[t]);
     }
 
-    // Epilogue: O = Õ / l -> bf16 -> swizzled smem (the dead Q tile) -> TMA store.
+    // Epilogue: O = Õ / l -> bf16 -> swizzled smem (the dead Q tile) -> TMA
+    // store. A tile that visited no key stores zeros (and LSE = -inf) once
+    // its Q tile, the staging area, has landed.
+    const bool tile_rows = row0 + t * kBM < Nq;
     if (ok && nt > 0)
       ok = mbar_wait_bounded(&bars.o_done[t], (nt - 1) & 1, abort_flag);
+    else if (ok)
+      ok = mbar_wait_bounded(&bars.q_full, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && nt > 0) {
+    if (ok && tile_rows) {
       tc::fence_after_sync();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
+        // (a tile that visited no key never wrote its Õ columns: zeros)
         uint32_t orr[32];
         tc::tmem_ld32(o_addr + ch * 32, orr);
         tc::tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
-                              __uint_as_float(orr[2 * e + 1]) * inv_l);
+          pk[e] = nt > 0 ? pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l,
+                                       __uint_as_float(orr[2 * e + 1]) * inv_l)
+                         : 0u;
         // 32 columns = 4 chunks of 16 bytes; atom = ch / 2, chunk index in row = (ch % 2) * 4 + u
         uint8_t* atom = stage + (ch / 2) * (kBM * 128) + r * 128;
 #pragma unroll
@@ -560,7 +623,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     }
     // Every warp of the warpgroup reaches this barrier, failed or not.
     named_bar_sync(1 + t, kBM);
-    if (nt > 0 && quarter == 0 && lane == 0 && !bars.abort) {
+    if (tile_rows && quarter == 0 && lane == 0 && !bars.abort) {
       uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
       for (int a = 0; a < C::kAtoms; ++a)
         tma_store_3d(&map_o, stage + a * (kBM * 128), 64 * a, row0 + t * kBM, bh);
@@ -576,7 +639,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   }
 }
 
-template <int D>
+template <int D, bool kGeneral>
 cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
   using C = FwdCfg<D>;
   CUtensorMap mq, mk, mv, mo;
@@ -585,7 +648,7 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
       !make_map_bf16_3d(&mv, a.v, D, a.Nk, uint64_t(a.B) * a.Hkv, kBN) ||
       !make_map_bf16_3d(&mo, a.o, D, a.Nq, uint64_t(a.B) * a.Hq, kBM))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, kGeneral>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   const int n_qblk = (a.Nq + 2 * kBM - 1) / (2 * kBM);
@@ -601,15 +664,19 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D>, mq, mk, mv, mo, a.lse, a.Hq, a.Hkv, a.Nq,
-                            a.Nk, a.scale, a.causal, n_qblk,
-                            order_group(a.causal != 0, 4LL * a.Nk * D));
+  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, kGeneral>, mq, mk, mv, mo, a.lse, a.Hq, a.Hkv, a.Nq,
+                            a.Nk, a.scale, a.mask, n_qblk,
+                            order_group(a.mask.varies(), 4LL * a.Nk * D));
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
-  return a.d == 64 ? launch_fwd_tc_d<64>(a) : launch_fwd_tc_d<128>(a);
+  const MaskSpec& m = a.mask;
+  const bool plain = m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
+                     m.row_kv_start == nullptr;   // no mask, or causal
+  if (plain) return a.d == 64 ? launch_fwd_tc_d<64, false>(a) : launch_fwd_tc_d<128, false>(a);
+  return a.d == 64 ? launch_fwd_tc_d<64, true>(a) : launch_fwd_tc_d<128, true>(a);
 }
 
 }  // namespace attn

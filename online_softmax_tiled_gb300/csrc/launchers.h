@@ -10,6 +10,19 @@
 
 namespace attn {
 
+// Attention mask (attn_mask in attn.h): key j is visible to query row i iff
+// it lies in the row's window around i' = i + Nk - Nq (a negative bound is
+// absent) or among the first n_global keys, and, when row ranges are given,
+// in [row_kv_start[b, i], row_kv_end[b, i]). Default: every key visible.
+struct MaskSpec {
+  int window_left = -1, window_right = -1, n_global = 0;
+  const int* row_kv_start = nullptr;   // [B, Nq] int32, device
+  const int* row_kv_end = nullptr;     // [B, Nq] int32, device
+  // work per query tile falls along the sequence (causal-like): CTA order
+  // puts the heaviest tiles first
+  bool varies() const { return window_right >= 0 || window_left >= 0 || row_kv_start != nullptr; }
+};
+
 struct FwdArgs {
   const void* q;
   const void* k;
@@ -21,6 +34,7 @@ struct FwdArgs {
   int causal;
   attn_dtype dt;
   cudaStream_t stream;
+  MaskSpec mask;      // the full mask (causal: window (-1, 0))
 };
 
 struct BwdArgs {

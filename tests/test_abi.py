@@ -32,6 +32,7 @@ def test_header_declares_the_boundary():
     names = set(_declared_functions())
     assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_decode_splitkv",
             "attn_decode_workspace_size", "attn_decode_paged", "attn_merge_partials",
+            "attn_fwd_masked",
             "attn_status_string", "attn_sync_status"} <= names
 
 
@@ -89,6 +90,9 @@ def _fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=2, Nq=16, Nk=16, d=64, s
     (dict(Nk=-1), INVALID),
     (dict(dt=7), INVALID),
     (dict(scale=float("nan")), INVALID),
+    (dict(scale=0.0), INVALID),                 # the kernels take row maxima before scaling
+    (dict(scale=-0.5), INVALID),
+    (dict(scale=float("inf")), INVALID),
     (dict(q=P + 2), MISALIGNED),
     (dict(lse=P + 4), MISALIGNED),
 ])
@@ -162,3 +166,18 @@ def test_product_path_does_not_import_oracle():
         files += [os.path.join(dirpath, f) for f in names if f.endswith(".py")]
     for f in files:
         assert not imp.search(open(f).read()), f
+
+
+def test_fwd_masked_rejects_before_launch(lib):
+    from online_softmax_tiled_gb300 import AttnMask
+
+    def call(mask=None, scale=0.125, Nq=16, Nk=16, d=64, q=P):
+        m = None if mask is None else ctypes.byref(mask)
+        return lib.attn_fwd_masked(q, P, P, P, P, 1, 2, 2, Nq, Nk, d, scale, m, 1, None)
+    half = AttnMask(-1, 0, 0, P, None)                  # only one of the two row-range arrays
+    assert call(half) == INVALID
+    assert call(AttnMask(-1, 0, 0, P + 2, P)) == MISALIGNED
+    assert call(AttnMask(-1, 0, 0, None, None), scale=0.0) == INVALID
+    assert call(AttnMask(3, 0, 0, None, None), d=96) == UNSUPPORTED
+    assert call(q=None) == INVALID
+    assert call(AttnMask(-1, 0, 0, None, None), q=P + 8) == MISALIGNED

@@ -40,6 +40,17 @@ class Workload:
     num_splits: int = 1
     seed: int = 0
     page_size: int = 0  # paged decode only: tokens per KV block
+    # general mask (forward): window around the diagonal (-1: unbounded),
+    # keys visible to every row, packed documents of this mean length
+    window_left: int = -1
+    window_right: int = -1
+    n_global: int = 0
+    doc_mean: int = 0
+
+    @property
+    def masked(self) -> bool:
+        return self.window_left >= 0 or self.n_global > 0 or self.doc_mean > 0 or (
+            self.window_right >= 0 and not self.causal)
 
     @property
     def scale(self) -> float:
@@ -60,6 +71,12 @@ WORKLOADS = {
                                       "bf16", causal=True),
     "decode_gqa_l4096": Workload("decode_gqa_l4096", "decode", 64, 32, 8, 1, 4096, 128, "bf16",
                                  num_splits=16),
+    # The long-context forward shape under a causal sliding window of 1024
+    # keys, and causal within packed documents of mean length 1024.
+    "fwd_swa_n8192_d128_w1024": Workload("fwd_swa_n8192_d128_w1024", "fwd", 2, 32, 32, 8192, 8192,
+                                         128, "bf16", window_left=1023, window_right=0),
+    "fwd_docs_n8192_d128": Workload("fwd_docs_n8192_d128", "fwd", 2, 32, 32, 8192, 8192, 128,
+                                    "bf16", window_right=0, doc_mean=1024, seed=1),
     # The GQA decode shape over a paged cache of 16-token blocks, with ragged
     # request lengths of mean 4096.
     "decode_paged_gqa_l4096": Workload("decode_paged_gqa_l4096", "decode_paged", 64, 32, 8, 1,
@@ -117,6 +134,25 @@ def make_paged_inputs(w: Workload, seq_lens=None, spare_pages: int = 3):
     dt = w.torch_dtype
     return {"q": q.to(dt), "k_pages": kp.to(dt), "v_pages": vp.to(dt), "block_table": table,
             "seq_lens": seq_lens}
+
+
+def make_doc_bounds(B: int, N: int, mean_len: int, seed: int):
+    """Documents packed back to back in each of B sequences of N tokens:
+    lengths drawn uniformly from [1, 2·mean_len - 1] (the last one cut at N).
+    Returns int32 CPU tensors row_kv_start, row_kv_end [B, N]: the key range
+    [start, end) of each token's document."""
+    g = torch.Generator().manual_seed(seed)
+    start = torch.empty((B, N), dtype=torch.int32)
+    end = torch.empty((B, N), dtype=torch.int32)
+    for b in range(B):
+        s = 0
+        while s < N:
+            n = int(torch.randint(1, 2 * mean_len, (1,), generator=g))
+            e = min(N, s + n)
+            start[b, s:e] = s
+            end[b, s:e] = e
+            s = e
+    return start, end
 
 
 def random_like_shape(shape, dtype: torch.dtype, seed: int, scale: float = 1.0):
