@@ -97,7 +97,8 @@ def algorithmic_units(w, inputs=None):
         bytes_ = 2 * w.B * w.Hkv * w.Nk * w.d * 2 + 2 * w.B * w.Hq * w.d * 2
         return bytes_, "GB/s", "hbm"
     if w.masked:
-        return 4.0 * w.Hq * w.d * visible_pairs(w, inputs), "TFLOP/s", "tensor"
+        flops = 4.0 * w.Hq * w.d * visible_pairs(w, inputs)
+        return flops * (2.5 if w.kind == "bwd" else 1.0), "TFLOP/s", "tensor"
     if w.causal:
         shift = w.Nk - w.Nq
         pairs = sum(min(w.Nk, i + shift + 1) for i in range(w.Nq))
@@ -235,7 +236,10 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
     for b, h in heads:
         sl = lambda t, hh: to_f64(t[b:b + 1, hh:hh + 1])
         q, k, v = sl(inputs["q"], h), sl(inputs["k"], h // r), sl(inputs["v"], h // r)
-        if w.kind == "bwd":
+        if w.kind == "bwd" and w.masked:
+            oracle.attention_bwd_masked(q, k, v, sl(inputs["do"], h), w.scale, mask_spec(w, inputs))
+            done_units += per_head
+        elif w.kind == "bwd":
             oracle.attention_bwd(q, k, v, sl(inputs["do"], h), w.scale, w.causal)
             done_units += per_head
         elif w.masked:
@@ -417,12 +421,18 @@ def run_gpu(args, w):
         launches_per_step = 1
         outs = (o, lse)
     elif w.kind == "bwd":
-        o, lse = ost.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale)
+        amask = (ost.make_mask(w.window_left, w.window_right, w.n_global) if w.masked
+                 else None)
+        o, lse = ost.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, mask=amask)
         ws = torch.empty(ost.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d),
                          dtype=torch.uint8, device=dev)
         dq, dk, dv = (torch.empty_like(x[n]) for n in ("q", "k", "v"))
-        step = lambda: ost.attn_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, dq, dk, dv,
-                                    w.scale, w.causal, ws, stream)
+        if w.masked:
+            step = lambda: ost.attn_bwd_masked(x["q"], x["k"], x["v"], o, x["do"], lse, dq, dk,
+                                               dv, w.scale, amask, ws, stream)
+        else:
+            step = lambda: ost.attn_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, dq, dk, dv,
+                                        w.scale, w.causal, ws, stream)
         launches_per_step = 3
         outs = (dq, dk, dv)
     elif w.kind == "decode_paged":

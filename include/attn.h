@@ -167,6 +167,20 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
                      attn_dtype dt, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * attn_bwd under a general mask (see attn_mask; mask == NULL: no mask): the
+ * same mask the forward used, so P is zero on every hidden (row, key) pair
+ * and on rows that see no key (LSE = -inf). Any Nq, Nk > 0; with dt =
+ * ATTN_BF16 and a mask other than none or causal, Nq is limited to 65536
+ * (d = 128) or 131072 (d = 64): ATTN_ERR_UNSUPPORTED beyond. Otherwise as
+ * attn_bwd, with the same workspace.
+ */
+ATTN_API attn_status attn_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dO, const float* lse, void* dq, void* dk,
+                                     void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                     float scale, const attn_mask* mask, attn_dtype dt,
+                                     void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Bytes of device scratch attn_decode_splitkv needs: per (b, query head,
  * split) the partial triple (o [d], m, l) in float32, 256-byte aligned.
  */

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     AttnError,
     AttnMask,
     attn_bwd,
+    attn_bwd_masked,
     attn_bwd_workspace_size,
     attn_decode_paged,
     attn_decode_splitkv,

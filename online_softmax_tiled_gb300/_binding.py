@@ -48,6 +48,9 @@ _SIGNATURES = {
                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "attn_fwd_masked": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 +
                         [ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
+    "attn_bwd_masked": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 +
+                        [ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                         ctypes.c_size_t, ctypes.c_void_p]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 6),
     "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 +
                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
@@ -172,6 +175,20 @@ def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, worksp
     _check(st, "attn_bwd")
 
 
+def attn_bwd_masked(q, k, v, o, do, lse, dq, dk, dv, scale: float, mask, workspace,
+                    stream=None):
+    """attn_bwd under an ``attn_mask`` (``make_mask``; None: no mask)."""
+    _device_contig(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    m = None if mask is None else ctypes.byref(mask)
+    st = lib().attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                               _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, d, float(scale), m, _dt(q),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check(st, "attn_bwd_masked")
+
+
 def attn_decode_workspace_size(B, Hq, d, num_splits) -> int:
     return int(lib().attn_decode_workspace_size(B, Hq, d, num_splits))
 
@@ -255,14 +272,18 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, with_lse:
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
-             stream=None):
-    """dQ, dK, dV by recomputation from the forward's O and LSE."""
+             stream=None, mask: AttnMask | None = None):
+    """dQ, dK, dV by recomputation from the forward's O and LSE (``mask``, the
+    forward's mask, replaces ``causal`` when given)."""
     B, Hq, Nq, d = q.shape
     scale = d ** -0.5 if scale is None else scale
     ws = torch.empty(attn_bwd_workspace_size(B, Hq, k.shape[1], Nq, k.shape[2], d),
                      dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, ws, stream)
+    if mask is not None:
+        attn_bwd_masked(q, k, v, o, do, lse, dq, dk, dv, scale, mask, ws, stream)
+    else:
+        attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal, ws, stream)
     return dq, dk, dv
 
 

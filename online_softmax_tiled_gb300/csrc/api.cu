@@ -144,12 +144,12 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   return bwd_layout(B, Hq, Nq, d).total;
 }
 
-attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
-                     int Nq, int Nk, int d, float scale, int causal, attn_dtype dt,
-                     void* workspace, size_t ws_bytes, void* stream) {
-  attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, causal, dt);
-  if (st != ATTN_OK) return st;
+namespace {
+
+attn_status bwd_common(const void* q, const void* k, const void* v, const void* o,
+                       const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int Nq, int Nk, int d, float scale, const MaskSpec& ms,
+                       attn_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return ATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
@@ -158,10 +158,18 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   const BwdLayout lay = bwd_layout(B, Hq, Nq, d);
   if (!workspace || ws_bytes < lay.total) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  const bool plain = ms.window_left < 0 && ms.window_right <= 0 && ms.n_global == 0 &&
+                     ms.row_kv_start == nullptr;
+  // general masks on the tensor-core key-tile pass list at most 1024 query
+  // tiles (64 rows at d = 128, 128 rows at d = 64) per key tile
+  if (!plain && dt == ATTN_BF16 && (Nq + (d == 128 ? 64 : 128) - 1) / (d == 128 ? 64 : 128) > 1024)
+    return ATTN_ERR_UNSUPPORTED;
+  const int causal = (plain && ms.window_right == 0) ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
   BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, causal, dt,
             reinterpret_cast<float*>(ws + lay.row_term), reinterpret_cast<float*>(ws + lay.dq_acc),
             static_cast<cudaStream_t>(stream), true};
+  a.mask = ms;
   // bf16, d = 128: a key-tile pass (dK, dV) and a query-tile pass (dQ, written
   // in bf16 directly; the float32 accumulator is not used). Otherwise one
   // pass adds dQ into the float32 accumulator, converted at the end.
@@ -177,6 +185,32 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   e = (dt == ATTN_BF16) ? launch_bwd_tc(a) : launch_bwd_simt(a);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return from_cuda(launch_bwd_convert(a));
+}
+
+}  // namespace
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, attn_dtype dt,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, causal, dt);
+  if (st != ATTN_OK) return st;
+  MaskSpec ms;
+  if (causal) ms.window_right = 0;
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale, ms, dt,
+                    workspace, ws_bytes, stream);
+}
+
+attn_status attn_bwd_masked(const void* q, const void* k, const void* v, const void* o,
+                            const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                            const attn_mask* mask, attn_dtype dt, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  attn_status st = check_attention_shapes(B, Hq, Hkv, Nq, Nk, d, 0, dt);
+  if (st != ATTN_OK) return st;
+  if ((st = check_mask(mask)) != ATTN_OK) return st;
+  return bwd_common(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Nq, Nk, d, scale,
+                    mask_spec(mask), dt, workspace, ws_bytes, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int d, int num_splits) {

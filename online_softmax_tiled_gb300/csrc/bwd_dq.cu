@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "mask.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -106,17 +107,21 @@ ATTN_DEVINL int key_tiles_for(int row_first, int Nq, int Nk, int causal) {
   return min(nk_tiles, (row_last + (Nk - Nq)) / kBN + 1);
 }
 
+// kGeneral = false: no mask or causal only; true: any MaskSpec (the key
+// tiles of the plan, per-element visibility as 32-bit masks).
+template <bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
               const float* __restrict__ row_term, int Hq, int Hkv, int Nq, int Nk, float scale,
-              int causal, int n_qt, int order_grp) {
+              MaskSpec mask, int n_qt, int order_grp) {
   using C = DqCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ DqBars bars;
+  __shared__ PlanSlots plan_slots;   // (no per-row slots: the dynamic buffers leave no room)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Causal: heads in groups whose K/V fit in L2 together, and in a group the
@@ -128,9 +133,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
   const int row0 = qt * kBM;
-  const int n = key_tiles_for(row0, Nq, Nk, causal);
-
   if (tid == 0) {
+    plan_slots.init();
     bars.abort = 0;
     mbar_init(&bars.q_full, 1);
     for (int i = 0; i < kKStages; ++i) {
@@ -161,6 +165,31 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
+  // Key tiles to visit: 0 .. n-1 (no mask, causal), or the plan of the
+  // mask (direct without row ranges; a reduction over the rows with them).
+  int n;
+  if (!kGeneral) {
+    n = key_tiles_for(row0, Nq, Nk, mask.window_right == 0);
+  } else {
+    PlanSlots slots;
+    if (mask.row_kv_start == nullptr) {
+      slots = plan_slots_direct(mask, row0, kBM, 1, Nq, Nk);
+      if (tid == 0) plan_slots = slots;   // the producer thread reads it back
+    } else {
+      if (warp >= 4 && warp < 8) {
+        // (the ranges are inputs, complete before the plainly launched
+        // preprocess started, and this grid starts after that)
+        plan_add_rows(&plan_slots, row_keys(mask, b, row0 + (warp - 4) * 32 + lane, Nq, Nk), 0);
+      }
+      __syncthreads();
+      slots = plan_slots;
+    }
+    n = slots.last[0] >= 0 ? make_plan(slots, kBN).count_upto(slots.last[0] / kBN) : 0;
+  }
+  auto key_tile = [&](int j) {
+    return kGeneral ? make_plan_volatile(&plan_slots, kBN).tile(j) : j;
+  };
+
   // Register split, set inside each role: 128 x 80 (TMA, MMA, idle warps) +
   // 256 x 208 (softmax) <= 384 x 168 registers the CTA is launched with.
   if (warp == 0) {
@@ -184,14 +213,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         mbar_arrive_expect_tx(&bars.k_full[sk], C::kTile);
         for (int a = 0; a < kD / 64; ++a)
           tc::tma_load_3d(smem + C::kOffK + sk * C::kTile + a * (kBN * 128), &map_k, 64 * a,
-                          j * kBN, kvh, &bars.k_full[sk]);
+                          key_tile(j) * kBN, kvh, &bars.k_full[sk]);
         ++issued_k;
         if (j >= kVStages) ok = mbar_wait_bounded(&bars.v_empty[sv], ((j / kVStages) - 1) & 1, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&bars.v_full[sv], C::kTile);
         for (int a = 0; a < kD / 64; ++a)
           tc::tma_load_3d(smem + C::kOffV + sv * C::kTile + a * (kBN * 128), &map_v, 64 * a,
-                          j * kBN, kvh, &bars.v_full[sv]);
+                          key_tile(j) * kBN, kvh, &bars.v_full[sv]);
         ++issued_v;
       }
       if (!ok) {
@@ -307,13 +336,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int row = row0 + r;
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const float c = scale * kLog2e;
-    const int shift = Nk - Nq;
     const bool row_in = row < Nq;
     const size_t ri = size_t(bh) * Nq + (row_in ? row : 0);
-    // rows past Nq: P = 0 (their dQ row is clipped by the store anyway)
-    const float nl = row_in ? -lse[ri] * kLog2e : -INFINITY;   // -LSE·log2e
-    const float nd = row_in ? -row_term[ri] : 0.f;             // -D
-    const int limit = causal ? min(Nk - 1, row + shift) : Nk - 1;   // last visible key
+    // rows past Nq and rows that see no key (LSE = -inf): P = 0
+    const float lse_r = row_in ? lse[ri] : -INFINITY;
+    const float nl = lse_r == -INFINITY ? -INFINITY : -lse_r * kLog2e;   // -LSE·log2e
+    const float nd = row_in ? -row_term[ri] : 0.f;                       // -D
+    const int limit = mask.window_right == 0 ? min(Nk - 1, row + (Nk - Nq)) : Nk - 1;
+    const RowKeys rk = kGeneral ? row_keys(mask, b, row, Nq, Nk) : RowKeys{1, 0, 1, 0};
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait2_warp(&bars.s_full[j & 1], (j >> 1) & 1, &bars.dp_full, j & 1, abort_flag)) {
@@ -332,10 +362,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tc::fence_before_sync();
       mbar_arrive(&bars.dp_free);                  // dP(j+1) may overwrite dP now
 
-      // Keys past the end (zero-filled K rows) and, for causal, after the
-      // row's limit contribute nothing.
-      const int key0 = j * kBN + half * 64;
-      const bool masked = key0 + 63 > limit;
+      // Keys this row does not see (past the end included) contribute
+      // nothing: a single limit without a general mask, 32-bit visibility
+      // masks with one.
+      const int key0 = (kGeneral ? make_plan_volatile(&plan_slots, kBN).tile(j) : j) * kBN +
+                       half * 64;
+      const bool masked = kGeneral ? !rk.covers(key0, key0 + 63) : key0 + 63 > limit;
+      const uint32_t vis0 = kGeneral && masked ? rk.bits(key0, 0) : 0xffffffffu;
+      const uint32_t vis1 = kGeneral && masked ? rk.bits(key0, 1) : 0xffffffffu;
       const f2 c2{c, c}, nl2{nl, nl}, nd2{nd, nd};
       uint32_t pk[32];                             // dS_j as bf16 pairs
 #pragma unroll
@@ -343,8 +377,14 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         const f2 x = fma2(f2{__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])}, c2, nl2);
         f2 p{fast_exp2(x.x), fast_exp2(x.y)};
         if (masked) {
-          if (key0 + 2 * e > limit) p.x = 0.f;
-          if (key0 + 2 * e + 1 > limit) p.y = 0.f;
+          if (kGeneral) {
+            const uint32_t vis = e < 16 ? vis0 : vis1;
+            if (!(vis & (1u << ((2 * e) & 31)))) p.x = 0.f;
+            if (!(vis & (1u << ((2 * e + 1) & 31)))) p.y = 0.f;
+          } else {
+            if (key0 + 2 * e > limit) p.x = 0.f;
+            if (key0 + 2 * e + 1 > limit) p.y = 0.f;
+          }
         }
         const f2 dpd = add2(f2{__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])}, nd2);
         const f2 ds = mul2(p, dpd);
@@ -420,7 +460,11 @@ cudaError_t launch_bwd_dq(const BwdArgs& a) {
       !make_map_bf16_3d(&mv, a.v, kD, a.Nk, bhk, kBN) ||
       !make_map_bf16_3d(&mdq, a.dq, kD, a.Nq, bhq, kBM))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const MaskSpec& m = a.mask;
+  const bool general = !(m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
+                         m.row_kv_start == nullptr);
+  const auto kern = general ? bwd_dq_kernel<true> : bwd_dq_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kDynSmem);
   if (e != cudaSuccess) return e;
   const int n_qt = (a.Nq + kBM - 1) / kBM;
@@ -440,10 +484,9 @@ cudaError_t launch_bwd_dq(const BwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_dq_kernel, mq, mk, mv, mdo, mdq, a.lse,
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, mdq, a.lse,
                             static_cast<const float*>(a.row_term), a.Hq, a.Hkv, a.Nq, a.Nk,
-                            a.scale, a.causal, n_qt,
-                            order_group(a.causal != 0, 4LL * a.Nk * kD));
+                            a.scale, a.mask, n_qt, order_group(m.varies(), 4LL * a.Nk * kD));
 }
 
 }  // namespace attn

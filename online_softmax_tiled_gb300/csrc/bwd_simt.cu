@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "mask.cuh"
 
 namespace attn {
 namespace {
@@ -35,7 +36,7 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
                 const T* __restrict__ dO, const float* __restrict__ lse,
                 const float* __restrict__ row_term, float* __restrict__ dq_acc,
                 T* __restrict__ dk, T* __restrict__ dv, int Hq, int Hkv, int Nq, int Nk,
-                float scale, int causal) {
+                float scale, MaskSpec mask) {
   extern __shared__ float smem[];
   float* sK = smem;                      // [kB][D+1]
   float* sV = sK + kB * (D + 1);         // [kB][D+1]
@@ -69,9 +70,13 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
   for (int c = 0; c < DC; ++c) dk_acc[c] = dv_acc[c] = 0.f;
 
-  // First query row that can see key kv0 (bottom-right causal alignment).
+  // First query row that can see key kv0: with a plain causal mask
+  // (bottom-right alignment) the earlier tiles are skipped; other masks
+  // visit every query tile and mask per pair.
+  const bool plain_causal = mask.window_left < 0 && mask.window_right == 0 &&
+                            mask.n_global == 0 && mask.row_kv_start == nullptr;
   int q_begin = 0;
-  if (causal) q_begin = max(0, kv0 - shift) / kB * kB;
+  if (plain_causal) q_begin = max(0, kv0 - shift) / kB * kB;
 
   for (int hh = 0; hh < group; ++hh) {
     const int h = g * group + hh;
@@ -110,12 +115,12 @@ bwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
       }
       const int row = q0 + ti;
       const float l_i = sL[ti], d_i = sD[ti];
+      const RowKeys rk = row_keys(mask, b, row, Nq, Nk);   // nothing for rows past Nq
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int j = tc + 4 * c;
         const int col = kv0 + j;
-        const bool vis = row < Nq && col < Nk && (!causal || col <= row + shift) &&
-                         l_i != -INFINITY;
+        const bool vis = rk.visible(col) && l_i != -INFINITY;
         const float p = vis ? expf(s[c] * scale - l_i) : 0.f;
         sP[ti * (kB + 1) + j] = p;
         sS[ti * (kB + 1) + j] = p * (dp[c] - d_i);
@@ -169,7 +174,7 @@ cudaError_t launch_bwd_simt_t(const BwdArgs& a) {
   bwd_simt_kernel<T, D><<<grid, kThreads, smem, a.stream>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k), static_cast<const T*>(a.v),
       static_cast<const T*>(a.dO), a.lse, a.row_term, a.dq_acc, static_cast<T*>(a.dk),
-      static_cast<T*>(a.dv), a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.causal);
+      static_cast<T*>(a.dv), a.Hq, a.Hkv, a.Nq, a.Nk, a.scale, a.mask);
   return cudaGetLastError();
 }
 

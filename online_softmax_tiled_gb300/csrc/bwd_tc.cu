@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "mask.cuh"
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -176,31 +177,85 @@ ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* do
 }
 
 // The (head, query tile) steps of one CTA: every query head of the group,
-// query tiles from the first one that sees key k0 (causal) to the last.
+// and per head the query tiles from the first one that sees key k0 (causal)
+// to the last, or (general masks) the query tiles listed in shared memory.
+constexpr int kMaxListedQTiles = 1024;
 struct StepPlan {
   int first_tile, tiles_per_head, group, n;
+  const unsigned short* list;   // general masks: query tiles, ascending
   ATTN_DEVINL void init(int k0, int Nq, int Nk, int causal, int group_, int BQ) {
     group = group_;
+    list = nullptr;
     const int nq_tiles = (Nq + BQ - 1) / BQ;
     first_tile = 0;
     if (causal) first_tile = max(0, k0 - (Nk - Nq)) / BQ;
     tiles_per_head = max(0, nq_tiles - first_tile);
     n = (k0 < Nk) ? tiles_per_head * group : 0;
   }
+  ATTN_DEVINL void init_listed(const unsigned short* list_, int count, int group_, int k0, int Nk) {
+    group = group_;
+    list = list_;
+    first_tile = 0;
+    tiles_per_head = count;
+    n = (k0 < Nk) ? count * group : 0;
+  }
   ATTN_DEVINL void at(int s, int& hh, int& qt) const {
     hh = s / tiles_per_head;
-    qt = first_tile + s % tiles_per_head;
+    qt = list != nullptr ? int(list[s % tiles_per_head]) : first_tile + s % tiles_per_head;
   }
 };
 
-template <int D>
+// General masks: the query tiles (of BQ rows) with a row that sees a key of
+// [k0, k1], listed ascending in `list`; returns their number. All threads of
+// the CTA call this (it has two barriers).
+template <int kThreadsT>
+ATTN_DEVINL int list_query_tiles(const MaskSpec& m, int b, int k0, int k1, int Nq, int Nk, int BQ,
+                                 uint32_t* bits, unsigned short* list, int* count) {
+  const int tid = threadIdx.x;
+  const int nq_tiles = (Nq + BQ - 1) / BQ;
+  const int words = (nq_tiles + 31) / 32;
+  for (int w = tid; w < words; w += kThreadsT) bits[w] = 0u;
+  __syncthreads();
+  for (int i = tid; i < Nq; i += kThreadsT) {
+    const RowKeys r = row_keys(m, b, i, Nq, Nk);
+    const bool sees = (r.lo1 <= r.hi1 && r.lo1 <= k1 && r.hi1 >= k0) ||
+                      (r.lo2 <= r.hi2 && r.lo2 <= k1 && r.hi2 >= k0);
+    if (sees) atomicOr(&bits[(i / BQ) >> 5], 1u << ((i / BQ) & 31));
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // words <= kMaxListedQTiles / 32 = 32: one word per lane
+    const uint32_t wbits = tid < words ? bits[tid] : 0u;
+    const int cnt = __popc(wbits);
+    int before = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, before, off);
+      if (tid >= off) before += t;
+    }
+    before -= cnt;
+    uint32_t x = wbits;
+    for (int k = 0; x != 0u; ++k) {
+      const int bit = __ffs(x) - 1;
+      list[before + k] = (unsigned short)(tid * 32 + bit);
+      x &= x - 1u;
+    }
+    if (tid == 31) *count = before + cnt;
+  }
+  __syncthreads();
+  return *count;
+}
+
+// kGeneral = false: no mask or causal only; true: any MaskSpec (listed query
+// tiles, per-step row key intervals, per-element masking of straddling steps).
+template <int D, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
               const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
               const float* __restrict__ lse, const float* __restrict__ row_term,
-              float* __restrict__ dq_acc, int Hq, int Hkv, int Nq, int Nk, float scale, int causal,
-              int n_ktiles, int order_grp) {
+              float* __restrict__ dq_acc, int Hq, int Hkv, int Nq, int Nk, float scale,
+              MaskSpec mask, int n_ktiles, int order_grp) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
   // The dQ pass that follows (d = 128) reads none of this kernel's outputs:
@@ -210,6 +265,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ BwdBars bars;
+  // general masks: the listed query tiles, and per stage the key intervals of
+  // its rows plus whether every (row, key) pair of the step is visible
+  __shared__ uint32_t qtile_bits[kGeneral ? kMaxListedQTiles / 32 : 1];
+  __shared__ unsigned short qtile_list[kGeneral ? kMaxListedQTiles : 1];
+  __shared__ int qtile_count;
+  __shared__ int4 stage_keys[kGeneral ? C::kQStages : 1][kGeneral ? BQ : 1];
+  __shared__ int stage_clean[kGeneral ? C::kQStages : 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Causal: KV heads in groups whose Q/dO fit in L2 together, and in a group
@@ -222,8 +284,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const int group = Hq / Hkv;
   const int k0 = ktile * kBK;
   StepPlan plan;
-  plan.init(k0, Nq, Nk, causal, group, BQ);
-  const int n = plan.n;
+  if (!kGeneral) plan.init(k0, Nq, Nk, mask.window_right == 0, group, BQ);
 
   if (tid == 0) {
     bars.abort = 0;
@@ -266,6 +327,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   tc::fence_after_sync();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
+  if (kGeneral) {
+    // (the row ranges are inputs: complete before the plainly launched
+    // preprocess started, and this grid starts after that)
+    const int cnt = list_query_tiles<kThreads>(mask, b, k0, min(k0 + kBK - 1, Nk - 1), Nq, Nk,
+                                               BQ, qtile_bits, qtile_list, &qtile_count);
+    plan.init_listed(qtile_list, cnt, group, k0, Nk);
+  }
+  const int n = plan.n;
 
   // Register split, set inside each role (launch: 512 x 128): warps 0-3
   // (TMA, MMA, LSE/D loader, idle) 120; the two Pᵀ/dSᵀ warpgroups 136 each;
@@ -328,7 +397,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       for (int u = 0; u < kPer; ++u) {
         const int q = qt * BQ + u * 32 + lane;
         const bool in = q < Nq;
-        nl[u] = in ? -lse[bh * Nq + q] * kLog2e : -INFINITY;
+        const float l = in ? lse[bh * Nq + q] : -INFINITY;   // -inf: the row sees no key
+        nl[u] = l == -INFINITY ? -INFINITY : -l * kLog2e;
         nd[u] = in ? -row_term[bh * Nq + q] : 0.f;
       }
     };
@@ -373,6 +443,23 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           vec[u * 32 + lane] = nl[u];
           vec[BQ + u * 32 + lane] = nd[u];
         }
+      }
+      if (kGeneral) {
+        // the key intervals of the step's rows; the step is clean if every
+        // row sees every key of the tile (rows past Nq have P = 0 anyway)
+        int hh, qt;
+        plan.at(s, hh, qt);
+        bool clean = k0 + kBK - 1 < Nk;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int q = qt * BQ + u * 32 + lane;
+          const RowKeys rq = row_keys(mask, b, q, Nq, Nk);
+          store_row_keys(&stage_keys[st][u * 32 + lane], rq);
+          clean &= q >= Nq || rq.covers(k0, k0 + kBK - 1);
+        }
+        clean = __all_sync(0xffffffffu, clean);
+        if (lane == 0) stage_clean[st] = clean ? 1 : 0;
+        __syncwarp();
       }
       mbar_arrive(&bars.q_full[st]);
       if (s + 1 < n) fetch(s + 1);
@@ -503,9 +590,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * BQ * 4);
       uint8_t* dst = smem + C::kOffP;
       const bool key_in = key < Nk;
-      // first visible query column of this key row (causal), relative to q0
-      const int qmin = causal ? key - shift - q0 : -1;
-      const bool masked_row = !key_in || qmin > cbase;
+      // first visible query column of this key row (causal), relative to q0;
+      // general masks: the step is masked unless every pair is visible
+      const int qmin = (!kGeneral && mask.window_right == 0) ? key - shift - q0 : -1;
+      const bool masked_row = kGeneral ? stage_clean[st] == 0 : (!key_in || qmin > cbase);
       const f2 c2{c, c};
 #pragma unroll
       for (int chunk = 0; chunk < CW / 32; ++chunk) {
@@ -533,8 +621,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               f2 p{fast_exp2(x.x), fast_exp2(x.y)};
               if (masked_row) {
                 const int col = col0 + e;
-                if (!key_in || col < qmin) p.x = 0.f;
-                if (!key_in || col + 1 < qmin) p.y = 0.f;
+                if (kGeneral) {
+                  if (!load_row_keys(&stage_keys[st][col]).visible(key)) p.x = 0.f;
+                  if (!load_row_keys(&stage_keys[st][col + 1]).visible(key)) p.y = 0.f;
+                } else {
+                  if (!key_in || col < qmin) p.x = 0.f;
+                  if (!key_in || col + 1 < qmin) p.y = 0.f;
+                }
               }
               const f2 dpd = add2(f2{__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])},
                                   u == 0 ? f2{nd.x, nd.y} : f2{nd.z, nd.w});
@@ -659,7 +752,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   }
 }
 
-template <int D>
+template <int D, bool kGeneral>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
@@ -671,21 +764,21 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
       !make_map_bf16_3d(&mdk, a.dk, D, a.Nk, bhk, kBK) ||
       !make_map_bf16_3d(&mdv, a.dv, D, a.Nk, bhk, kBK))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D, kGeneral>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   const int n_ktiles = (a.Nk + kBK - 1) / kBK;
   // Q and dO of every query head of a KV head are re-read by all its key
   // tiles; groups of up to 64 MiB of them (measured: one group of 32 heads
   // of 2 MB ran 2 % faster than two groups of 16)
-  const int order_grp = order_group(a.causal != 0, 4LL * a.Nq * D * (a.Hq / a.Hkv), 64LL << 20);
+  const int order_grp = order_group(a.mask.varies(), 4LL * a.Nq * D * (a.Hq / a.Hkv), 64LL << 20);
   const long blocks = long(n_ktiles) * a.B * a.Hkv;
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
   if (C::kFusedDq) {
     // d = 64 adds into the accumulator the preprocess zeroes: plain launch
-    bwd_tc_kernel<D><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
+    bwd_tc_kernel<D, kGeneral><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
         mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk,
-        a.scale, a.causal, n_ktiles, order_grp);
+        a.scale, a.mask, n_ktiles, order_grp);
     return cudaGetLastError();
   }
   // d = 128: programmatic dependent of the preprocess; only the LSE/D loader
@@ -701,15 +794,19 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D>, mq, mk, mv, mdo, mdk, mdv, a.lse,
+  return cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, kGeneral>, mq, mk, mv, mdo, mdk, mdv, a.lse,
                             static_cast<const float*>(a.row_term), a.dq_acc, a.Hq, a.Hkv, a.Nq,
-                            a.Nk, a.scale, a.causal, n_ktiles, order_grp);
+                            a.Nk, a.scale, a.mask, n_ktiles, order_grp);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_tc(const BwdArgs& a) {
-  return a.d == 64 ? launch_bwd_tc_d<64>(a) : launch_bwd_tc_d<128>(a);
+  const MaskSpec& m = a.mask;
+  const bool plain = m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
+                     m.row_kv_start == nullptr;   // no mask, or causal
+  if (plain) return a.d == 64 ? launch_bwd_tc_d<64, false>(a) : launch_bwd_tc_d<128, false>(a);
+  return a.d == 64 ? launch_bwd_tc_d<64, true>(a) : launch_bwd_tc_d<128, true>(a);
 }
 
 }  // namespace attn

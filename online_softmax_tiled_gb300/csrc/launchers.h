@@ -55,6 +55,7 @@ struct BwdArgs {
   float* dq_acc;     // float32 dQ accumulator, [B, Hq, Nq, d]
   cudaStream_t stream;
   bool zero_dq_acc;  // the preprocess zeroes dq_acc (the passes that add into it)
+  MaskSpec mask;     // the full mask (causal: window (-1, 0))
 };
 
 struct DecodeArgs {

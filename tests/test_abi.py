@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     names = set(_declared_functions())
     assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_decode_splitkv",
             "attn_decode_workspace_size", "attn_decode_paged", "attn_merge_partials",
-            "attn_fwd_masked",
+            "attn_fwd_masked", "attn_bwd_masked",
             "attn_status_string", "attn_sync_status"} <= names
 
 
@@ -181,3 +181,20 @@ def test_fwd_masked_rejects_before_launch(lib):
     assert call(AttnMask(3, 0, 0, None, None), d=96) == UNSUPPORTED
     assert call(q=None) == INVALID
     assert call(AttnMask(-1, 0, 0, None, None), q=P + 8) == MISALIGNED
+
+
+def test_bwd_masked_rejects_before_launch(lib):
+    from online_softmax_tiled_gb300 import AttnMask
+    need = lib.attn_bwd_workspace_size(1, 2, 2, 16, 16, 64)
+
+    def call(mask, Nq=16, d=64, dt=1, ws=P, ws_bytes=need, scale=0.125):
+        m = None if mask is None else ctypes.byref(mask)
+        return lib.attn_bwd_masked(*([P] * 9), 1, 2, 2, Nq, 16, d, scale, m, dt, ws, ws_bytes,
+                                   None)
+    assert call(AttnMask(-1, 0, 0, P, None)) == INVALID
+    assert call(AttnMask(-1, 0, 0, P, P + 1)) == MISALIGNED
+    assert call(AttnMask(7, 0, 0, None, None), ws_bytes=need - 1) == WORKSPACE
+    assert call(AttnMask(7, 0, 0, None, None), scale=-1.0) == INVALID
+    # a general bf16 mask lists at most 1024 query tiles per key tile
+    big = lib.attn_bwd_workspace_size(1, 2, 2, 70000, 16, 128)
+    assert call(AttnMask(7, 0, 0, None, None), Nq=70000, d=128, ws_bytes=big) == UNSUPPORTED

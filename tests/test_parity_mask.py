@@ -105,3 +105,86 @@ def test_causal_mask_equals_causal_call_bitwise(ost, d):
     o2, l2 = ost.forward(x["q"], x["k"], x["v"], scale=w.scale, mask=ost.make_mask(-1, 0, 0))
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ------------------------------------------------------------- backward
+
+def _grads_masked(ost, w, spec, rows=None):
+    """GPU gradients under the mask (O and LSE from the GPU forward, as a
+    training step would) and the oracle's."""
+    x = {k: t.to(DEV) for k, t in make_inputs(w).items()}
+    rs = re = None
+    if rows is not None:
+        rs, re = rows[0].to(DEV), rows[1].to(DEV)
+    mask = ost.make_mask(spec.get("window_left", -1), spec.get("window_right", -1),
+                         spec.get("n_global", 0), rs, re)
+    o, lse = ost.forward(x["q"], x["k"], x["v"], scale=w.scale, mask=mask)
+    grads = ost.backward(x["q"], x["k"], x["v"], o, x["do"], lse, scale=w.scale, mask=mask)
+    torch.cuda.synchronize()
+    ospec = dict(spec)
+    if rows is not None:
+        ospec["row_kv_start"], ospec["row_kv_end"] = rows[0].numpy(), rows[1].numpy()
+    ref = oracle.attention_bwd_masked(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]),
+                                      to_f64(x["do"]), w.scale, ospec)
+    return grads, ref
+
+
+def _check_grads(ost, w, spec, rows=None):
+    grads, ref = _grads_masked(ost, w, spec, rows)
+    tol = 5e-2 if w.dtype == "bf16" else 1e-4
+    ospec = dict(spec)
+    if rows is not None:
+        ospec["row_kv_start"], ospec["row_kv_end"] = rows[0].numpy(), rows[1].numpy()
+    # query rows that see no key and keys no row sees take part in no pair:
+    # their gradients are exactly zero
+    seen = np.stack([oracle.attention._mask_of(ospec, b, w.Nq, w.Nk) for b in range(w.B)])
+    lonely = {"dq": ~seen.any(axis=2), "dk": ~seen.any(axis=1), "dv": ~seen.any(axis=1)}
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        got = to_f64(g)
+        assert np.all(np.isfinite(got)), name
+        scale_ref = max(np.max(np.abs(r)), 1e-30)
+        assert np.max(np.abs(got - r)) <= tol * scale_ref, (name, np.max(np.abs(got - r)),
+                                                             scale_ref)
+        sel = lonely[name][:, None, :].repeat(got.shape[1], axis=1)
+        assert np.all(got[sel] == 0), name
+
+
+BWD_DT = [("bf16", 128), ("bf16", 64), ("f32", 64)]
+
+
+@pytest.mark.parametrize("dtype,d", BWD_DT)
+@pytest.mark.parametrize("name", ["window100", "sinks4_window64", "prefix_lm77",
+                                  "local_both_sides"])
+def test_backward_window_and_global_masks(ost, dtype, d, name):
+    w = Workload("maskb", "bwd", 1, 4, 2, 400, 400, d, dtype, seed=7 + d + len(name))
+    _check_grads(ost, w, SPECS[name])
+
+
+@pytest.mark.parametrize("dtype,d", BWD_DT)
+def test_backward_document_mask(ost, dtype, d):
+    w = Workload("docsb", "bwd", 2, 2, 1, 520, 520, d, dtype, seed=31)
+    rows = make_doc_bounds(2, 520, 70, seed=9)
+    _check_grads(ost, w, {"window_left": -1, "window_right": 0}, rows)
+
+
+@pytest.mark.parametrize("dtype,d", BWD_DT)
+def test_backward_empty_rows_and_unequal_lengths(ost, dtype, d):
+    """Causal with Nq > Nk (rows that see nothing: LSE = -inf, zero dQ) and a
+    window whose early keys no query sees (zero dK, dV)."""
+    w = Workload("emptyb", "bwd", 1, 2, 2, 500, 300, d, dtype, seed=41)
+    _check_grads(ost, w, {"window_left": -1, "window_right": 0})
+    w2 = Workload("suffixb", "bwd", 1, 2, 1, 140, 700, d, dtype, seed=43)
+    _check_grads(ost, w2, {"window_left": 60, "window_right": 0})
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_causal_mask_equals_causal_call_bitwise(ost, d):
+    w = Workload("causalb", "bwd", 1, 4, 2, 600, 600, d, "bf16", seed=51)
+    x = {k: t.to(DEV) for k, t in make_inputs(w).items()}
+    o, lse = ost.forward(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
+    g1 = ost.backward(x["q"], x["k"], x["v"], o, x["do"], lse, causal=True, scale=w.scale)
+    g2 = ost.backward(x["q"], x["k"], x["v"], o, x["do"], lse, scale=w.scale,
+                      mask=ost.make_mask(-1, 0, 0))
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)

@@ -77,6 +77,9 @@ WORKLOADS = {
                                          128, "bf16", window_left=1023, window_right=0),
     "fwd_docs_n8192_d128": Workload("fwd_docs_n8192_d128", "fwd", 2, 32, 32, 8192, 8192, 128,
                                     "bf16", window_right=0, doc_mean=1024, seed=1),
+    # The causal backward shape under a sliding window of 1024 keys.
+    "bwd_swa_n4096_d128_w1024": Workload("bwd_swa_n4096_d128_w1024", "bwd", 2, 16, 16, 4096,
+                                         4096, 128, "bf16", window_left=1023, window_right=0),
     # The GQA decode shape over a paged cache of 16-token blocks, with ragged
     # request lengths of mean 4096.
     "decode_paged_gqa_l4096": Workload("decode_paged_gqa_l4096", "decode_paged", 64, 32, 8, 1,
