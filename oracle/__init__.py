@@ -33,6 +33,7 @@ from .attention import (  # noqa: F401
     merge_partials,
     gather_paged,
     decode_paged,
+    decode_sparse,
     decode_splitkv,
     default_scale,
 )

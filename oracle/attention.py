@@ -26,6 +26,10 @@ Sources, by page and section:
 * ML notes, prefill/decode and the KV cache: a serving cache is kept in
   fixed-size blocks reached through a per-request block table
   (``gather_paged``, ``decode_paged``).
+* ML notes, sparse-attention split-K kernel notes: T query tokens attend
+  over an arbitrary scattered list of KV positions chosen upstream (by an
+  indexer), gathered per tile; split-K partials merged exactly
+  (``decode_sparse``).
 * Flash Attention 2 post, §Causal masking, "Why": option A handles
   arbitrary masks (sliding window, document boundaries, prefix LM) as a
   0 / -inf term added to the scores before the online softmax
@@ -468,3 +472,34 @@ def decode_paged(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
 def default_scale(d: int) -> float:
     """1/sqrt(d), the score scaling of the ML notes' attention Q&A."""
     return 1.0 / math.sqrt(d)
+
+
+def decode_sparse(q: np.ndarray, k: np.ndarray, v: np.ndarray, indices: np.ndarray,
+                  counts: np.ndarray, scale: float):
+    """Attention of T query tokens per request over a scattered index list:
+    O [B, Hq, T, d], LSE [B, Hq, T].
+
+    ML notes, sparse-attention split-K notes: the kernel is given a list of
+    KV positions per request (selected upstream) and attends over exactly
+    those entries. Reading: one list per request, shared by its T tokens
+    and all heads; entry e of request b is cache row indices[b, e] for
+    e < counts[b]; a position listed twice counts twice (attention over the
+    gathered list). q: [B, Hq, T, d]; k, v: [B, Hkv, L, d]. An empty list
+    gives O = 0, LSE = -inf.
+    """
+    B, Hq, T, _ = q.shape
+    Hkv = k.shape[1]
+    o = np.zeros((B, Hq, T, v.shape[-1]))
+    lse = np.full((B, Hq, T), NEG_INF)
+    for b in range(B):
+        n = int(counts[b])
+        if n == 0:
+            continue
+        idx = np.asarray(indices[b, :n])
+        for h in range(Hq):
+            g = _kv_head(h, Hq, Hkv)
+            kk, vv = k[b, g, idx], v[b, g, idx]          # the gathered list
+            s = scale * (q[b, h] @ kk.T)                 # [T, n]
+            o[b, h] = softmax_rows(s) @ vv
+            lse[b, h] = logsumexp_rows(s)
+    return o, lse

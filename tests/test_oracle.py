@@ -722,3 +722,64 @@ def test_planted_mask_mistakes_are_caught(monkeypatch):
                 except Exception:
                     errs.append(np.inf)
             assert max(errs) > 1e-6, f"pins missed the planted mistake: {name}"
+
+
+# --------------------------------------------------------------------------
+# Sparse-index decode (T query tokens over a scattered index list)
+# --------------------------------------------------------------------------
+
+def _sparse_inputs(B=2, Hq=4, Hkv=2, T=3, L=40, d=5, n=11, seed=120):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, T, d))
+    k = rng.standard_normal((B, Hkv, L, d))
+    v = rng.standard_normal((B, Hkv, L, d))
+    idx = np.stack([rng.choice(L, size=n, replace=False) for _ in range(B)])
+    return q, k, v, idx
+
+
+def test_sparse_decode_brute_force():
+    """Pure-Python loops over the listed rows of each (request, head, token)."""
+    q, k, v, idx = _sparse_inputs()
+    counts = np.array([11, 7])
+    o, lse = oracle.decode_sparse(q, k, v, idx, counts, 0.8)
+    for b in range(2):
+        for h in range(4):
+            g = h // 2
+            rows = [int(j) for j in idx[b, :counts[b]]]
+            for t in range(3):
+                ob, lb = _brute_attention([q[b, h, t].tolist()], k[b, g, rows].tolist(),
+                                          v[b, g, rows].tolist(), 0.8, False)
+                np.testing.assert_allclose(o[b, h, t], ob[0], rtol=0, atol=1e-13)
+                assert abs(lse[b, h, t] - lb[0]) < 1e-13
+
+
+def test_sparse_decode_order_invariant_and_full_list_is_dense():
+    """The list's order does not matter; listing every position once is
+    ordinary (non-causal) attention over the whole cache."""
+    q, k, v, idx = _sparse_inputs(n=40, L=40)
+    counts = np.array([40, 40])
+    o1, l1 = oracle.decode_sparse(q, k, v, idx, counts, 0.6)
+    rng = np.random.default_rng(3)
+    idx2 = np.stack([rng.permutation(r) for r in idx])
+    o2, l2 = oracle.decode_sparse(q, k, v, idx2, counts, 0.6)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+    o3, l3 = oracle.attention_fwd(q, k, v, 0.6, False)
+    np.testing.assert_allclose(o1, o3, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l3, rtol=0, atol=1e-13)
+
+
+def test_sparse_decode_closed_forms():
+    """Empty list: O = 0, LSE = -inf. One entry: O = v_j, LSE = scale·q·k_j.
+    A position listed twice weighs twice: O = (2 e^s0 v0 + e^s1 v1) / (2 e^s0 + e^s1)."""
+    q, k, v, _ = _sparse_inputs(B=3, Hq=1, Hkv=1, T=1)
+    idx = np.array([[5, 0, 0], [9, 0, 0], [4, 4, 7]])
+    o, lse = oracle.decode_sparse(q, k, v, idx, np.array([0, 1, 3]), 0.7)
+    assert np.all(o[0] == 0) and lse[0, 0, 0] == -np.inf
+    np.testing.assert_allclose(o[1, 0, 0], v[1, 0, 9], rtol=1e-14)
+    assert abs(lse[1, 0, 0] - 0.7 * (q[1, 0, 0] @ k[1, 0, 9])) < 1e-13
+    s0, s1 = 0.7 * (q[2, 0, 0] @ k[2, 0, 4]), 0.7 * (q[2, 0, 0] @ k[2, 0, 7])
+    w0, w1 = np.exp(s0), np.exp(s1)
+    np.testing.assert_allclose(o[2, 0, 0], (2 * w0 * v[2, 0, 4] + w1 * v[2, 0, 7]) / (2 * w0 + w1),
+                               rtol=1e-12)
+    assert abs(lse[2, 0, 0] - np.log(2 * w0 + w1)) < 1e-12
