@@ -37,9 +37,11 @@ L2_BYTES = 129 << 20
 # ----------------------------------------------------------------- workload math
 
 def make_workload_inputs(w):
-    from workloads import make_doc_bounds, make_inputs, make_paged_inputs
+    from workloads import make_doc_bounds, make_inputs, make_paged_inputs, make_sparse_inputs
     if w.kind == "decode_paged":
         return make_paged_inputs(w)
+    if w.kind == "decode_sparse":
+        return make_sparse_inputs(w)
     x = make_inputs(w)
     if w.doc_mean > 0:
         x["row_kv_start"], x["row_kv_end"] = make_doc_bounds(w.B, w.Nq, w.doc_mean, w.seed + 1)
@@ -84,6 +86,14 @@ def paged_bytes(w, seq_lens):
             + 4 * (blocks + len(seq_lens)))
 
 
+def sparse_bytes(w, counts):
+    """Bytes a sparse-index decode must move: the K and V rows of every listed
+    entry once per KV head, the list entries and counts, q and o (T tokens)."""
+    n = sum(int(c) for c in counts)
+    return (2 * w.Hkv * n * w.d * 2 + 2 * len(counts) * w.Hq * w.Nq * w.d * 2
+            + 4 * (n + len(counts)))
+
+
 def algorithmic_units(w, inputs=None):
     """(per-step units, unit name, bound) for a workload.
 
@@ -93,6 +103,8 @@ def algorithmic_units(w, inputs=None):
     over each request's own length, plus its block-table entries)."""
     if w.kind == "decode_paged":
         return paged_bytes(w, inputs["seq_lens"].tolist()), "GB/s", "hbm"
+    if w.kind == "decode_sparse":
+        return sparse_bytes(w, inputs["counts"].tolist()), "GB/s", "hbm"
     if w.kind == "decode":
         bytes_ = 2 * w.B * w.Hkv * w.Nk * w.d * 2 + 2 * w.B * w.Hq * w.d * 2
         return bytes_, "GB/s", "hbm"
@@ -201,6 +213,19 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
     units_total, _, _ = algorithmic_units(w, inputs)
     t0 = time.perf_counter()
     done = 0
+    if w.kind == "decode_sparse":
+        cnt = inputs["counts"].numpy()
+        idx = inputs["indices"].numpy()
+        units = 0
+        for b in range(w.B):
+            oracle.decode_sparse(to_f64(inputs["q"][b:b + 1]), to_f64(inputs["k"][b:b + 1]),
+                                 to_f64(inputs["v"][b:b + 1]), idx[b:b + 1], cnt[b:b + 1],
+                                 w.scale)
+            units += sparse_bytes(w, cnt[b:b + 1].tolist())
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return units, time.perf_counter() - t0, f"{done} of {w.B} requests"
     if w.kind == "decode_paged":
         lens = inputs["seq_lens"].numpy()
         table = inputs["block_table"].numpy()
@@ -310,8 +335,12 @@ METRIC = "attn fwd/bwd TFLOP/s vs GB300 BF16 peak; split-KV decode GB/s vs HBM"
 def workload_config(w, flushed: bool):
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk,
            "d": w.d, "causal": w.causal, "dtype": w.dtype}
-    if w.kind in ("decode", "decode_paged"):
+    if w.kind in ("decode", "decode_paged", "decode_sparse"):
         cfg["num_splits"] = w.num_splits
+    if w.kind == "decode_sparse":
+        cfg["Nq"] = f"{w.Nq} query tokens per request"
+        cfg["Nk"] = f"cache of {w.Nk} rows per request"
+        cfg["n_index"] = f"{w.n_index} distinct rows listed per request, uniform, random order"
     if w.masked:
         cfg["mask"] = {"window_left": w.window_left, "window_right": w.window_right,
                        "n_global": w.n_global}
@@ -339,7 +368,7 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"fwd": "fwd_tc.cu", "bwd": "bwd_tc.cu", "decode": "decode.cu",
-                  "decode_paged": "decode.cu"}
+                  "decode_paged": "decode.cu", "decode_sparse": "decode.cu"}
 FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
@@ -353,6 +382,8 @@ def kernel_label(w):
         return "attn_bwd call (row-term preprocess + main kernel + dQ convert)"
     if w.kind == "decode_paged":
         return "attn_decode_paged call (split kernel + merge kernel)"
+    if w.kind == "decode_sparse":
+        return "attn_decode_sparse call (split kernel + merge kernel)"
     return "attn_decode_splitkv call (split kernel + merge kernel)"
 
 
@@ -435,6 +466,15 @@ def run_gpu(args, w):
                                         w.scale, w.causal, ws, stream)
         launches_per_step = 3
         outs = (dq, dk, dv)
+    elif w.kind == "decode_sparse":
+        ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq * w.Nq, w.d, w.num_splits),
+                         dtype=torch.uint8, device=dev)
+        o = torch.empty_like(x["q"])
+        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        step = lambda: ost.attn_decode_sparse(x["q"], x["k"], x["v"], x["indices"], x["counts"],
+                                              o, lse, w.scale, w.num_splits, ws, stream)
+        launches_per_step = 2
+        outs = (o, lse)
     elif w.kind == "decode_paged":
         ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq, w.d, w.num_splits),
                          dtype=torch.uint8, device=dev)

@@ -248,6 +248,37 @@ ATTN_API attn_status attn_decode_paged(const void* q, const void* k_pages, const
                               void* stream);
 
 /*
+ * Sparse-index split-KV decode: T query tokens per request attend over a
+ * scattered list of cache rows.
+ *
+ * ML notes (haolingpu.github.io), sparse-attention split-K notes: the list
+ * of KV positions is chosen upstream (an indexer); the kernel gathers the
+ * listed rows tile by tile into shared memory, splits the list across
+ * blocks and merges the (o, m, l) partials exactly. Reading: one list per
+ * request, shared by its T tokens and all heads; a row listed twice counts
+ * twice.
+ *
+ * q [B, Hq, T, d] bf16; k_cache/v_cache [B, Hkv, L, d] bf16; indices
+ * [B, max_idx] int32 and counts [B] int32 in DEVICE memory: request b
+ * attends over cache rows indices[b*max_idx + e], e < counts[b]; o
+ * [B, Hq, T, d] bf16 written; lse [B, Hq, T] float32 written (may be NULL).
+ * A request with an empty list gets O = 0, LSE = -inf. The list is cut into
+ * chunks of c = ceil(max_idx / num_splits) rounded up to 32 entries and at
+ * least 128 (num_splits is the most splits a request uses).
+ * Device-side checks: a count outside [0, max_idx] or a listed row outside
+ * [0, L) is never dereferenced; the request (bad count) or the chunk
+ * holding the bad row gets no keys and attn_sync_status() reports
+ * ATTN_ERR_DEVICE_INDEX. d 64 or 128; Hq/Hkv in {1, 2, 4, 8}; any T.
+ * workspace: attn_decode_workspace_size(B, Hq * T, d, num_splits) bytes,
+ * 256-byte aligned.
+ */
+ATTN_API attn_status attn_decode_sparse(const void* q, const void* k_cache, const void* v_cache,
+                                        const int* indices, const int* counts, void* o,
+                                        float* lse, int B, int Hq, int Hkv, int T, int L,
+                                        int max_idx, int d, float scale, int num_splits,
+                                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * The exact (o, m, l) merge on its own (ML notes, split-K notes; the
  * attention-residuals lab, "Phase 2: merge the live partial exactly").
  *

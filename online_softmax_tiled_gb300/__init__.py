@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     attn_bwd_masked,
     attn_bwd_workspace_size,
     attn_decode_paged,
+    attn_decode_sparse,
     attn_decode_splitkv,
     attn_decode_splitkv_noalloc,
     attn_decode_workspace_size,
@@ -27,6 +28,7 @@ from ._binding import (  # noqa: F401
     backward,
     decode,
     decode_paged,
+    decode_sparse,
     forward,
     lib,
     make_mask,

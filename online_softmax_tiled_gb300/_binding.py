@@ -62,6 +62,9 @@ _SIGNATURES = {
     "attn_decode_paged": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 7 +
                           [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                            ctypes.c_void_p]),
+    "attn_decode_sparse": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 7 +
+                           [ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                            ctypes.c_void_p]),
     "attn_merge_partials": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
                             [ctypes.c_void_p]),
     "attn_decode_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 +
@@ -237,6 +240,23 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale:
     _check(st, "attn_decode_paged")
 
 
+def attn_decode_sparse(q, k_cache, v_cache, indices, counts, o, lse, scale: float,
+                       num_splits: int, workspace, stream=None):
+    """q [B,Hq,T,d] bf16; caches [B,Hkv,L,d] bf16; indices [B,max_idx] and
+    counts [B] int32 on the device; o [B,Hq,T,d] bf16; lse [B,Hq,T] or None."""
+    _device_contig(q, k_cache, v_cache, indices, counts, o, lse, workspace)
+    if indices.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise TypeError("indices and counts must be int32")
+    B, Hq, T, d = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    st = lib().attn_decode_sparse(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices),
+                                  _ptr(counts), _ptr(o), _ptr(lse), B, Hq, Hkv, T, L,
+                                  indices.shape[1], d, float(scale), int(num_splits),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check(st, "attn_decode_sparse")
+
+
 def attn_merge_partials(o_part, m_part, l_part, o, lse, stream=None):
     """o_part [rows,S,d], m_part/l_part [rows,S] float32 -> o [rows,d], lse [rows]."""
     _device_contig(o_part, m_part, l_part, o, lse)
@@ -313,4 +333,19 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, num_splits: int,
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, scale, num_splits,
                       workspace, stream)
+    return o, lse
+
+
+def decode_sparse(q, k_cache, v_cache, indices, counts, num_splits: int,
+                  scale: float | None = None, stream=None, workspace=None):
+    """Sparse-index decode of T tokens per request: O [B,Hq,T,d] bf16, LSE [B,Hq,T]."""
+    B, Hq, T, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(B, Hq * T, d, num_splits),
+                                dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    attn_decode_sparse(q, k_cache, v_cache, indices, counts, o, lse, scale, num_splits, workspace,
+                       stream)
     return o, lse

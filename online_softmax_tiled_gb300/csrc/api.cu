@@ -289,6 +289,49 @@ attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_
   return from_cuda(launch_merge(decode_merge_args(a)));
 }
 
+attn_status attn_decode_sparse(const void* q, const void* k_cache, const void* v_cache,
+                               const int* indices, const int* counts, void* o, float* lse, int B,
+                               int Hq, int Hkv, int T, int L, int max_idx, int d, float scale,
+                               int num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || L <= 0 || max_idx <= 0 || d <= 0 ||
+      num_splits <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !indices || !counts || !o) return ATTN_ERR_INVALID_ARG;
+  if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
+  if (num_splits > 65535 || B > 65535 || max_idx > (1 << 30)) return ATTN_ERR_UNSUPPORTED;
+  // query rows (heads x tokens) and the CTAs over them stay in 32 bits; one
+  // CTA row group holds at least one row, so Hkv x G x T bounds the grid rows
+  const long long rows = 1LL * Hq * T;
+  if (rows * B > (1LL << 30) || 1LL * Hkv * G * T > 65535 ||
+      1LL * B * Hkv * G * T * num_splits > (1LL << 30))
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (lse && !aligned16(lse)) || (reinterpret_cast<uintptr_t>(indices) & 3u) ||
+      (reinterpret_cast<uintptr_t>(counts) & 3u))
+    return ATTN_ERR_MISALIGNED;
+  const DecodeLayout lay = decode_layout(B, int(rows), d, num_splits);
+  if (!workspace || ws_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
+  char* ws = static_cast<char*>(workspace);
+  DecodeArgs a{q, k_cache, v_cache, o, lse, B, Hq, Hkv, L, d, scale, num_splits,
+               reinterpret_cast<float*>(ws + lay.o_part), reinterpret_cast<float*>(ws + lay.m_part),
+               reinterpret_cast<float*>(ws + lay.l_part), static_cast<cudaStream_t>(stream)};
+  a.block_table = indices;
+  a.seq_lens = counts;
+  a.num_pages = L;          // a listed row must lie in [0, L)
+  a.page_size = 1;
+  a.max_pages = max_idx;
+  a.sparse = true;
+  a.T = T;
+  cudaError_t e = launch_decode_split(a);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  return from_cuda(launch_merge(decode_merge_args(a)));
+}
+
 attn_status attn_merge_partials(const float* o_part, const float* m_part, const float* l_part,
                                 void* o, float* lse, int rows, int num_splits, int d,
                                 attn_dtype out_dt, void* stream) {

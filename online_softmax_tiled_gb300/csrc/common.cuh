@@ -239,6 +239,19 @@ ATTN_DEVINL void grouped_tile_order(int block, int n_tiles, int n_heads, int gro
   rank = idx / hcount;
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, 16-byte aligned
+// addresses), and an arrival on an mbarrier once every cp.async this thread
+// issued before it has landed (the barrier's expected count includes it).
+ATTN_DEVINL void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src) : "memory");
+}
+ATTN_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+ATTN_DEVINL void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 ATTN_DEVINL void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

@@ -64,12 +64,16 @@ constexpr size_t decode_smem_bytes() {
   return ring > merge ? ring : merge;
 }
 
-// Paged cache: pages [num_pages][Hkv][page_size][D]; block_table
-// [B][max_pages]; seq_lens [B].
+// Gathered keys. Paged cache: pages [num_pages][Hkv][page_size][D];
+// block_table [B][max_pages]; seq_lens [B]. Sparse index list (rows = 1):
+// the cache stays [B][Hkv][L][D], block_table holds each request's listed
+// rows [B][max_pages], seq_lens the list lengths, page_size = 1 and
+// num_pages = L (every listed row is its own one-row page).
 struct PagedKV {
   const int* block_table;
   const int* seq_lens;
   int num_pages, page_size, max_pages;
+  int rows;   // 1: sparse index list into the per-request cache
 };
 
 template <int D, int G, bool kPaged>
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
-                    int L, int S, int chunk, float scale, PagedKV pg) {
+                    int L, int S, int chunk, float scale, PagedKV pg, int rgroups) {
   constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
   constexpr int kRowBytes = D * 2;
   constexpr int kStageBytes = kStageKeys * kRowBytes;
@@ -90,13 +94,19 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   __shared__ int abort_flag;
   __shared__ int chunk_pages[kPaged ? kChunkPagesCached : 1];
 
-  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // blockIdx.y = (KV head, group of G query rows); query row r of this CTA
+  // is row b·Hq + blockIdx.y·G + r (Hq counts query rows: heads x tokens)
+  const int s = blockIdx.x, gy = blockIdx.y, b = blockIdx.z;
+  const int g = gy / rgroups;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
 
+  // a sparse index list is gathered by every thread (cp.async), each
+  // arriving on the stage barrier; otherwise thread 0 issues bulk copies
+  const bool gather_all = kPaged && pg.rows != 0;
   if (tid == 0) {
     abort_flag = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], gather_all ? kThreads : 1);
     fence_barrier_init();
   }
   // Launched as a programmatic dependent: every global access of this grid
@@ -150,7 +160,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     // a page index out of range: the chunk reads nothing and leaves no mass
     if (tid == 0) attn_flag_error(kErrBadIndex);
     if (tid < G) {
-      const size_t row = size_t(b) * Hq + g * G + tid;
+      const size_t row = size_t(b) * Hq + gy * G + tid;
       m_part[row * S + s] = -INFINITY;
       l_part[row * S + s] = 0.f;
     }
@@ -162,12 +172,29 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   const int nstages = (nkeys + kStageKeys - 1) / kStageKeys;
 
   // Element offset of key t of (b, g) in the K and V arrays.
-  const size_t head_off = kPaged ? size_t(g) * pg.page_size * D
-                                 : (size_t(b) * Hkv + g) * size_t(L) * D;
-  const size_t page_elems = size_t(Hkv) * pg.page_size * D;     // paged only
+  const bool sparse = kPaged && pg.rows != 0;
+  const size_t head_off = kPaged && !sparse ? size_t(g) * pg.page_size * D
+                                            : (size_t(b) * Hkv + g) * size_t(L) * D;
+  const size_t page_elems = sparse ? size_t(D) : size_t(Hkv) * pg.page_size * D;   // gathers
   auto page_of = [&](int t) {
     const int i = t / pg.page_size - p_first;
     return i < kChunkPagesCached ? chunk_pages[i] : table_row[t / pg.page_size];
+  };
+  // Sparse list (all threads): 16-byte pieces, consecutive threads along a
+  // row, so a listed row is one coalesced 128- or 256-byte read per tensor.
+  auto gather = [&](int st) {
+    constexpr int kPieces = kRowBytes / 16;
+    const int buf = st % kStages;
+    const int t0 = key_begin + st * kStageKeys;
+    const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+    for (int p = tid; p < rows * 2 * kPieces; p += kThreads) {
+      const int r = p / (2 * kPieces), rem = p % (2 * kPieces);
+      const int tensor = rem / kPieces, piece = rem % kPieces;
+      const size_t off = head_off + size_t(page_of(t0 + r)) * page_elems;
+      const uint8_t* src = reinterpret_cast<const uint8_t*>((tensor ? v : k) + off) + piece * 16;
+      cp_async16((tensor ? sV : sK) + buf * kStageBytes + r * kRowBytes + piece * 16, src);
+    }
+    cp_async_mbar_arrive(&full_bar[buf]);
   };
   auto issue = [&](int st) {
     const int buf = st % kStages;
@@ -192,9 +219,12 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
       bulk_g2s(sV + buf * kStageBytes, v + off, uint32_t(rows) * kRowBytes, &full_bar[buf]);
     }
   };
-  int issued = 0;  // meaningful in thread 0 only
-  if (tid == 0)
+  int issued = 0;  // meaningful in thread 0 only (every thread when gathering)
+  if (gather_all) {
+    for (; issued < min(kStages, nstages); ++issued) gather(issued);
+  } else if (tid == 0) {
     for (; issued < min(kStages, nstages); ++issued) issue(issued);
+  }
 
   // Query slice of this lane for all G heads, pre-scaled into log2 units,
   // as pairs of consecutive dimensions (packed f32x2 arithmetic).
@@ -203,7 +233,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   const float qs = scale * kLog2e;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const __nv_bfloat16* qh = q + (size_t(b) * Hq + g * G + h) * D;
+    const __nv_bfloat16* qh = q + (size_t(b) * Hq + gy * G + h) * D;
 #pragma unroll
     for (int vv = 0; vv < NV; ++vv) {
       const uint4 w = *reinterpret_cast<const uint4*>(qh + 64 * vv + 8 * sub);
@@ -233,16 +263,23 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     // One barrier per stage: all threads agree on failure, and the buffer of
     // stage st-1 is free once every thread has arrived here.
     if (__syncthreads_or(fail)) {
-      if (tid == 0) {
+      // Let copies already issued land before shared memory goes away.
+      if (gather_all) {
+        cp_async_wait_all();
+        if (tid == 0) attn_flag_error(kErrTimeout);
+      } else if (tid == 0) {
         attn_flag_error(kErrTimeout);
-        // Let copies already issued land before shared memory goes away.
         for (int t = st; t < issued; ++t)
           mbar_wait_bounded(&full_bar[t % kStages], (t / kStages) & 1, nullptr);
       }
       ok = false;
       break;
     }
-    if (tid == 0 && issued < nstages && st >= 1) issue(issued++);
+    if (gather_all) {
+      if (issued < nstages && st >= 1) gather(issued++);
+    } else if (tid == 0 && issued < nstages && st >= 1) {
+      issue(issued++);
+    }
     const int rows = min(kStageKeys, nkeys - st * kStageKeys);
     const uint8_t* kb = sK + buf * kStageBytes;
     const uint8_t* vb = sV + buf * kStageBytes;
@@ -368,7 +405,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         l = fmaf(w, sm_l[t * G + h], l);
       }
     }
-    const size_t row = size_t(b) * Hq + g * G + h;
+    const size_t row = size_t(b) * Hq + gy * G + h;
     o_part[(row * S + s) * D + c] = o;
     if (c == 0) {
       m_part[row * S + s] = (mx == -INFINITY) ? -INFINITY : mx * kLn2;  // back to natural units
@@ -453,13 +490,13 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
 }
 
 template <int D, int G, bool kPaged>
-cudaError_t launch_split_t(const DecodeArgs& a) {
+cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
   const size_t smem = decode_smem_bytes<D, G>();
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, kPaged>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_splits, a.Hkv, a.B);
+  cfg.gridDim = dim3(a.num_splits, a.Hkv * rgroups, a.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
@@ -468,21 +505,35 @@ cudaError_t launch_split_t(const DecodeArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const PagedKV pg{a.block_table, a.seq_lens, a.num_pages, a.page_size, a.max_pages};
+  const PagedKV pg{a.block_table, a.seq_lens, a.num_pages, a.page_size, a.max_pages,
+                   a.sparse ? 1 : 0};
   return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, kPaged>,
                             static_cast<const __nv_bfloat16*>(a.q),
                             static_cast<const __nv_bfloat16*>(a.k),
                             static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part,
-                            a.Hq, a.Hkv, a.L, a.num_splits, decode_chunk(a), a.scale, pg);
+                            a.Hq * a.T, a.Hkv, a.L, a.num_splits, decode_chunk(a), a.scale, pg,
+                            rgroups);
 }
 
+// Query rows per KV head: (Hq / Hkv) x T. One CTA takes G of them (G = all
+// of them for single-token decode; with several tokens at most 4 at d = 128
+// and 8 at d = 64, the register budget of one CTA) and the rest go to
+// further CTAs over the same keys.
 template <int D, bool kPaged>
 cudaError_t launch_split_d(const DecodeArgs& a) {
-  switch (a.Hq / a.Hkv) {
-    case 1: return launch_split_t<D, 1, kPaged>(a);
-    case 2: return launch_split_t<D, 2, kPaged>(a);
-    case 4: return launch_split_t<D, 4, kPaged>(a);
-    case 8: return launch_split_t<D, 8, kPaged>(a);
+  const int rows = (a.Hq / a.Hkv) * a.T;
+  int G = rows;
+  if (a.T > 1) {
+    const int cap = D == 128 ? 4 : 8;
+    G = 1;
+    while (G * 2 <= cap && rows % (G * 2) == 0) G *= 2;
+  }
+  const int rgroups = rows / G;
+  switch (G) {
+    case 1: return launch_split_t<D, 1, kPaged>(a, rgroups);
+    case 2: return launch_split_t<D, 2, kPaged>(a, rgroups);
+    case 4: return launch_split_t<D, 4, kPaged>(a, rgroups);
+    case 8: return launch_split_t<D, 8, kPaged>(a, rgroups);
     default: return cudaErrorInvalidValue;
   }
 }

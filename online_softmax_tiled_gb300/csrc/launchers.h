@@ -77,6 +77,11 @@ struct DecodeArgs {
   const int* block_table = nullptr;
   const int* seq_lens = nullptr;
   int num_pages = 0, page_size = 0, max_pages = 0;
+  // Sparse index list (sparse): block_table = listed rows [B, max_pages] of
+  // the contiguous cache, seq_lens = list lengths, page_size = 1,
+  // num_pages = L. T query tokens per request: q, o [B, Hq, T, d].
+  bool sparse = false;
+  int T = 1;
 };
 
 struct MergeArgs {
@@ -99,19 +104,23 @@ struct MergeArgs {
 // Keys per decode chunk: ceil(L / S) for a contiguous cache; for a paged
 // cache one length for all requests, the table's capacity over S rounded up
 // to whole 32-key stages, so request b uses ceil(n_b / chunk) <= S chunks.
+// A sparse index list has chunks of at least 128 entries (four 32-entry
+// stages): smaller ones leave each CTA too little work to cover its start.
 inline int decode_chunk(const DecodeArgs& a) {
   if (a.block_table == nullptr) return (a.L + a.num_splits - 1) / a.num_splits;
   const long long cap = 1LL * a.max_pages * a.page_size;
-  const long long c = (cap + a.num_splits - 1) / a.num_splits;
-  return int((c + 31) / 32 * 32);
+  long long c = (cap + a.num_splits - 1) / a.num_splits;
+  c = (c + 31) / 32 * 32;
+  if (a.sparse && c < 128) c = 128;
+  return int(c);
 }
 
 // The merge that completes a decode call.
 inline MergeArgs decode_merge_args(const DecodeArgs& a) {
-  MergeArgs m{a.o_part, a.m_part, a.l_part, a.o, a.lse, a.B * a.Hq, a.num_splits, a.d,
+  MergeArgs m{a.o_part, a.m_part, a.l_part, a.o, a.lse, a.B * a.Hq * a.T, a.num_splits, a.d,
               ATTN_BF16, a.stream};
   m.seq_lens = a.seq_lens;
-  m.Hq = a.Hq;
+  m.Hq = a.Hq * a.T;   // query rows per request
   m.len = a.L;
   m.max_len = a.block_table != nullptr ? a.max_pages * a.page_size : a.L;
   m.chunk = decode_chunk(a);

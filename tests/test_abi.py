@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     names = set(_declared_functions())
     assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_decode_splitkv",
             "attn_decode_workspace_size", "attn_decode_paged", "attn_merge_partials",
-            "attn_fwd_masked", "attn_bwd_masked",
+            "attn_fwd_masked", "attn_bwd_masked", "attn_decode_sparse",
             "attn_status_string", "attn_sync_status"} <= names
 
 
@@ -198,3 +198,18 @@ def test_bwd_masked_rejects_before_launch(lib):
     # a general bf16 mask lists at most 1024 query tiles per key tile
     big = lib.attn_bwd_workspace_size(1, 2, 2, 70000, 16, 128)
     assert call(AttnMask(7, 0, 0, None, None), Nq=70000, d=128, ws_bytes=big) == UNSUPPORTED
+
+
+def test_decode_sparse_rejects_before_launch(lib):
+    def call(B=2, Hq=8, Hkv=2, T=4, L=100, n=50, d=128, S=4, ws=P, ws_bytes=None, idx=P):
+        need = lib.attn_decode_workspace_size(B, Hq * T, d, S) if ws_bytes is None else ws_bytes
+        return lib.attn_decode_sparse(P, P, P, idx, P, P, P, B, Hq, Hkv, T, L, n, d, 0.1, S, ws,
+                                      need, None)
+    assert call(T=0) == INVALID
+    assert call(n=0) == INVALID
+    assert call(idx=None) == INVALID
+    assert call(Hq=6, Hkv=4) == INVALID
+    assert call(Hq=32, Hkv=2) == UNSUPPORTED     # group of 16
+    assert call(d=96) == UNSUPPORTED
+    assert call(ws_bytes=lib.attn_decode_workspace_size(2, 8, 128, 4)) == WORKSPACE  # T ignored
+    assert call(idx=P + 2) == MISALIGNED

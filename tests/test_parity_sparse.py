@@ -1,0 +1,104 @@
+"""GPU sparse-index decode vs the float64 oracle.
+
+T query tokens per request attend over a scattered list of cache rows (ML
+notes, sparse-attention split-K notes). Tolerance as for decode (benchmark
+description): bf16 O max|err| <= 2e-2, LSE <= 1e-3.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, Workload, make_inputs, make_sparse_inputs, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+ATTN_ERR_DEVICE_INDEX = -7
+
+
+def _run(ost, w, x):
+    o, lse = ost.decode_sparse(x["q"], x["k"], x["v"], x["indices"], x["counts"], w.num_splits,
+                               w.scale)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _oracle(w, x):
+    return oracle.decode_sparse(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]),
+                                x["indices"].cpu().numpy(), x["counts"].cpu().numpy(), w.scale)
+
+
+def _check(ost, w, counts=None, x=None):
+    if x is None:
+        x = {k: t.to(DEV) for k, t in make_sparse_inputs(w, counts).items()}
+    o, lse = _run(ost, w, x)
+    o_ref, lse_ref = _oracle(w, x)
+    got_o, got_lse = to_f64(o), to_f64(lse)
+    assert np.max(np.abs(got_o - o_ref)) <= 2e-2
+    empty = np.isneginf(lse_ref)
+    assert np.all(np.isneginf(got_lse[empty])) and np.all(got_o[empty] == 0)
+    assert np.max(np.abs(got_lse[~empty] - lse_ref[~empty]), initial=0.0) <= 1e-3
+
+
+def test_sparse_workload_full(ost):
+    """B=8, Hq=Hkv=16, T=8, 2048 of 16384 rows listed per request, 32 splits:
+    every output row."""
+    _check(ost, WORKLOADS["decode_sparse_t8_i2048"])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,L,d,n,S,counts", [
+    (2, 4, 4, 8, 900, 128, 300, 7, None),         # T = 8, 4 rows per CTA, 2 row groups
+    (3, 8, 2, 3, 500, 128, 257, 5, [257, 0, 31]), # 12 rows per KV head: groups of 4; empty list
+    (2, 8, 1, 2, 700, 64, 130, 4, [1, 130]),      # group of 8 x 2 tokens at d = 64
+    (1, 2, 2, 1, 333, 128, 200, 16, None),        # single token: plain decode over the list
+    (2, 16, 16, 5, 600, 64, 64, 3, [64, 33]),     # T = 5: one row per CTA group
+])
+def test_small_shapes(ost, B, Hq, Hkv, T, L, d, n, S, counts):
+    w = Workload("sparse", "decode_sparse", B, Hq, Hkv, T, L, d, "bf16", num_splits=S,
+                 seed=B + T + n, n_index=n)
+    _check(ost, w, counts)
+
+
+def test_duplicates_and_list_order(ost):
+    """A row listed twice counts twice; the order of the list does not matter."""
+    w = Workload("dup", "decode_sparse", 2, 4, 2, 4, 300, 128, "bf16", num_splits=4, seed=5,
+                 n_index=96)
+    x = {k: t.to(DEV) for k, t in make_sparse_inputs(w).items()}
+    x["indices"][:, 48:] = x["indices"][:, :48]          # every row twice
+    _check(ost, w, x=x)
+    o1, l1 = _run(ost, w, x)
+    perm = torch.randperm(96, generator=torch.Generator().manual_seed(1)).to(DEV)
+    x["indices"] = x["indices"][:, perm].contiguous()
+    o2, l2 = _run(ost, w, x)
+    assert torch.max(torch.abs(o1.float() - o2.float())) <= 2e-2
+    assert torch.max(torch.abs(l1 - l2)) <= 1e-4
+
+
+def test_full_list_equals_dense_decode(ost):
+    """Listing every row once in order is ordinary split-KV decode (T = 1)."""
+    w = Workload("full", "decode", 3, 8, 2, 1, 640, 128, "bf16", num_splits=5, seed=8)
+    x = {k: t.to(DEV) for k, t in make_inputs(w).items()}
+    o_ref, lse_ref = ost.decode(x["q"], x["k"], x["v"], w.num_splits, w.scale)
+    idx = torch.arange(640, dtype=torch.int32, device=DEV).repeat(3, 1).contiguous()
+    cnt = torch.full((3,), 640, dtype=torch.int32, device=DEV)
+    o, lse = ost.decode_sparse(x["q"][:, :, None], x["k"], x["v"], idx, cnt, w.num_splits,
+                               w.scale)
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(o[:, :, 0].float() - o_ref.float())) <= 1e-2
+    assert torch.max(torch.abs(lse[:, :, 0] - lse_ref)) <= 1e-4
+
+
+def test_out_of_range_rows_are_flagged_not_read(ost):
+    w = Workload("bad", "decode_sparse", 3, 4, 2, 2, 400, 128, "bf16", num_splits=4, seed=9,
+                 n_index=128)
+    x = {k: t.to(DEV) for k, t in make_sparse_inputs(w).items()}
+    o_ref, lse_ref = _oracle(w, x)
+    x["indices"][1, 70] = 400          # past the cache
+    x["counts"][2] = 129               # past the list
+    o, lse = _run(ost, w, x)
+    assert ost.attn_sync_status() == ATTN_ERR_DEVICE_INDEX
+    got_o, got_lse = to_f64(o), to_f64(lse)
+    assert np.max(np.abs(got_o[0] - o_ref[0])) <= 2e-2
+    assert np.max(np.abs(got_lse[0] - lse_ref[0])) <= 1e-3
+    assert np.all(got_o[2] == 0) and np.all(np.isneginf(got_lse[2]))

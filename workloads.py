@@ -46,6 +46,7 @@ class Workload:
     window_right: int = -1
     n_global: int = 0
     doc_mean: int = 0
+    n_index: int = 0    # sparse-index decode: listed rows per request (Nq = tokens T)
 
     @property
     def masked(self) -> bool:
@@ -80,6 +81,11 @@ WORKLOADS = {
     # The causal backward shape under a sliding window of 1024 keys.
     "bwd_swa_n4096_d128_w1024": Workload("bwd_swa_n4096_d128_w1024", "bwd", 2, 16, 16, 4096,
                                          4096, 128, "bf16", window_left=1023, window_right=0),
+    # Sparse-index decode as the ML notes' split-K kernel notes describe it:
+    # T = 8 query tokens, 16 heads, 2048 listed rows per request, 32 splits;
+    # 8 requests with caches of 16384 rows.
+    "decode_sparse_t8_i2048": Workload("decode_sparse_t8_i2048", "decode_sparse", 8, 16, 16, 8,
+                                       16384, 128, "bf16", num_splits=32, n_index=2048),
     # The GQA decode shape over a paged cache of 16-token blocks, with ragged
     # request lengths of mean 4096.
     "decode_paged_gqa_l4096": Workload("decode_paged_gqa_l4096", "decode_paged", 64, 32, 8, 1,
@@ -137,6 +143,22 @@ def make_paged_inputs(w: Workload, seq_lens=None, spare_pages: int = 3):
     dt = w.torch_dtype
     return {"q": q.to(dt), "k_pages": kp.to(dt), "v_pages": vp.to(dt), "block_table": table,
             "seq_lens": seq_lens}
+
+
+def make_sparse_inputs(w: Workload, counts=None):
+    """Seeded CPU tensors for sparse-index decode: q [B, Hq, T, d]; k, v
+    [B, Hkv, L, d] drawn N(0, 1); per request n_index distinct rows drawn
+    uniformly from [0, L) in random order (indices [B, n_index] int32);
+    counts [B] int32 (all n_index unless given)."""
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn((w.B, w.Hq, w.Nq, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=g, dtype=torch.float32)
+    idx = torch.stack([torch.randperm(w.Nk, generator=g)[:w.n_index] for _ in range(w.B)])
+    cnt = torch.full((w.B,), w.n_index) if counts is None else torch.as_tensor(counts)
+    dt = w.torch_dtype
+    return {"q": q.to(dt), "k": k.to(dt), "v": v.to(dt), "indices": idx.to(torch.int32),
+            "counts": cnt.to(torch.int32)}
 
 
 def make_doc_bounds(B: int, N: int, mean_len: int, seed: int):
