@@ -122,6 +122,24 @@ def algorithmic_units(w, inputs=None):
     return flops, "TFLOP/s", "tensor"
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the whole job's time is its slowest
+    rank's); x itself on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float, unit: str) -> float:
+    """Throughput of the whole job: every rank processed units_per_rank (weak
+    scaling, independent replicas) in at most `seconds`."""
+    return rate(world * units_per_rank, seconds, unit)
+
+
 def rate(units, seconds, unit):
     return units / seconds / (1e12 if unit == "TFLOP/s" else 1e9)
 
@@ -540,10 +558,7 @@ def run_gpu(args, w):
         sampler.mark_end()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     assert ost.attn_sync_status(stream) == ost.ATTN_OK
 
     # --- end to end through the public API: pinned host inputs in, results out
@@ -571,16 +586,13 @@ def run_gpu(args, w):
     e_e.record(stream)
     barrier()
     e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     clocks = sampler.stop() if sampler else None
 
     if rank == 0:
         ms_per_step = total_ms / args.steps
-        value = rate(world * units * args.steps, total_ms / 1e3, unit)
+        value = whole_job_rate(units * args.steps, world, total_ms / 1e3, unit)
         hbm, tf_burst, tf_sust, src = load_peaks()
         peak = hbm if bound == "hbm" else tf_burst
         peak_source = f"{src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops burst'})"
@@ -602,7 +614,7 @@ def run_gpu(args, w):
             "cpu_baseline": {"value": rate(cpu_units, cpu_s, unit), "unit": unit,
                              "cores": host_cores(), "kind": "oracle",
                              "sample": f"{cpu_desc} of one step, float64 NumPy, {cpu_s:.1f} s"},
-            "e2e": {"value": rate(world * units, e2e_ms / 1e3, unit), "unit": unit,
+            "e2e": {"value": whole_job_rate(units, world, e2e_ms / 1e3, unit), "unit": unit,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
