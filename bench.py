@@ -392,7 +392,8 @@ FP32_FFMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 def kernel_label(w):
     if w.kind == "fwd":
-        return ("fwd_simt_kernel" if w.dtype == "f32" else "fwd_tc_kernel") + \
+        return ("fwd_simt_kernel" if w.dtype == "f32" else
+                "fwd_tc64_kernel (persistent)" if w.d == 64 else "fwd_tc_kernel") + \
             " (whole attn_fwd call, one launch)"
     if w.kind == "bwd":
         if w.dtype == "bf16" and w.d == 128:
@@ -405,9 +406,16 @@ def kernel_label(w):
     return "attn_decode_splitkv call (split kernel + merge kernel)"
 
 
-def kernel_source_sha(kind):
+def kernel_source(w):
+    """Source file of the workload's dominant kernel."""
+    if w.kind == "fwd" and w.dtype == "bf16" and w.d == 64:
+        return "fwd_tc64.cu"
+    return KERNEL_SOURCES[w.kind]
+
+
+def kernel_source_sha(w):
     import hashlib
-    path = os.path.join(ROOT, "online_softmax_tiled_gb300", "csrc", KERNEL_SOURCES[kind])
+    path = os.path.join(ROOT, "online_softmax_tiled_gb300", "csrc", kernel_source(w))
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -421,7 +429,7 @@ def profiled_traffic(w):
         return None
     with open(path) as f:
         entry = json.load(f).get(w.name)
-    if not entry or entry.get("source_sha") != kernel_source_sha(w.kind):
+    if not entry or entry.get("source_sha") != kernel_source_sha(w):
         return None
     return entry.get("dram_bytes_per_launch")
 

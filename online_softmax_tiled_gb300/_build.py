@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(REPO_DIR, "_build")
 LIB_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libattn_gb300.so")
 
-SOURCES = ["api.cu", "fwd_simt.cu", "fwd_tc.cu", "bwd_aux.cu", "bwd_simt.cu", "bwd_tc.cu",
+SOURCES = ["api.cu", "fwd_simt.cu", "fwd_tc.cu", "fwd_tc64.cu", "bwd_aux.cu", "bwd_simt.cu", "bwd_tc.cu",
            "bwd_dq.cu", "decode.cu"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -348,8 +348,8 @@ attn_status attn_merge_partials(const float* o_part, const float* m_part, const 
 attn_status attn_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
-  const uint32_t w =
-      take_error_fwd_tc() | take_error_bwd_tc() | take_error_bwd_dq() | take_error_decode();
+  const uint32_t w = take_error_fwd_tc() | take_error_fwd_tc64() | take_error_bwd_tc() |
+                     take_error_bwd_dq() | take_error_decode();
   if (w == 0xffffffffu) return ATTN_ERR_CUDA;
   if (w & kErrTimeout) return ATTN_ERR_DEVICE_TIMEOUT;
   if (w & kErrBadIndex) return ATTN_ERR_DEVICE_INDEX;

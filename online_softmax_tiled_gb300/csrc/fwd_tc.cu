@@ -672,6 +672,7 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
 }  // namespace
 
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
+  if (a.d == 64) return launch_fwd_tc64(a);   // persistent kernel (fwd_tc64.cu)
   const MaskSpec& m = a.mask;
   const bool plain = m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
                      m.row_kv_start == nullptr;   // no mask, or causal

@@ -141,6 +141,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 cudaError_t launch_fwd_simt(const FwdArgs& a);
 cudaError_t launch_fwd_tc(const FwdArgs& a);
+cudaError_t launch_fwd_tc64(const FwdArgs& a);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a);
 cudaError_t launch_bwd_simt(const BwdArgs& a);
 cudaError_t launch_bwd_tc(const BwdArgs& a);
@@ -151,6 +152,7 @@ cudaError_t launch_merge(const MergeArgs& a);
 
 // Per-translation-unit device error words (read and cleared).
 uint32_t take_error_fwd_tc();
+uint32_t take_error_fwd_tc64();
 uint32_t take_error_bwd_tc();
 uint32_t take_error_bwd_dq();
 uint32_t take_error_decode();
