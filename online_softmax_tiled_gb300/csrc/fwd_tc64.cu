@@ -48,12 +48,13 @@ constexpr int D = 64;
 constexpr int kBM = 128;            // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;            // keys per K/V tile
 constexpr int kThreads = 384;       // 12 warps
-constexpr int kStages = 4;          // K/V ring
+constexpr int kKStages = 6;         // K ring (a stage is released by the QKᵀ that reads it)
+constexpr int kVStages = 4;         // V ring (released later, by the P̃V)
 constexpr int kTileBytes = kBM * D * 2;                  // Q, K, V or O tile (16 KB)
 constexpr int kQOff = 0;                                 // Q buffers 0, 1
 constexpr int kKOff = 2 * kTileBytes;
-constexpr int kVOff = kKOff + kStages * kTileBytes;
-constexpr int kOOff = kVOff + kStages * kTileBytes;      // O staging
+constexpr int kVOff = kKOff + kKStages * kTileBytes;
+constexpr int kOOff = kVOff + kVStages * kTileBytes;     // O staging
 constexpr int kSmemBytes = kOOff + kTileBytes;
 constexpr int kDynSmem = kSmemBytes + 1024;              // slack for 1024-byte alignment
 // TMEM columns of warpgroup t: S_t, Õ_t, P̃_t
@@ -64,9 +65,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: Õ is rescaled when m grows > 2^8
 
+// One query tile of the work list and the key tiles it visits.
+struct TileWork {
+  int bh, kvh, row0;
+  int n;                 // key tiles visited (plan indices 0 .. n-1)
+  KeyTilePlan plan;      // plan index -> key tile (general masks)
+};
+
 struct Bars {
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t w_free[2];    // the softmax warpgroups have read work slot 0 / 1
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
   uint64_t o_free;
   uint64_t mma_drain[2];
@@ -74,6 +83,9 @@ struct Bars {
   int abort;
   int stop;         // the softmax warpgroups' joint decision to leave the tile loop
   PlanSlots plan;   // keys the tile's rows see (general masks with row ranges)
+  // Tile k's work, written by the Q/K producer with its Q load into slot
+  // k % 2 (the index arithmetic is done once per tile, off the softmax path)
+  TileWork work[2];
 };
 
 ATTN_DEVINL void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1,
@@ -105,12 +117,19 @@ ATTN_DEVINL void tmem_st32(uint32_t ta, const uint32_t (&r)[32]) {
       : "memory");
 }
 
-// One query tile of the work list and the key tiles it visits.
-struct TileWork {
-  int bh, kvh, row0;
-  int n;                 // key tiles visited (plan indices 0 .. n-1)
-  KeyTilePlan plan;      // plan index -> key tile (general masks)
-};
+ATTN_DEVINL TileWork read_work(const TileWork* slot) {
+  const volatile TileWork* v = slot;
+  TileWork tw;
+  tw.bh = v->bh;
+  tw.kvh = v->kvh;
+  tw.row0 = v->row0;
+  tw.n = v->n;
+  tw.plan.s0 = v->plan.s0;
+  tw.plan.n0 = v->plan.n0;
+  tw.plan.s1 = v->plan.s1;
+  tw.plan.n1 = v->plan.n1;
+  return tw;
+}
 
 // Key-tile steps of softmax warpgroup t (plan indices t, t + 2, ...).
 ATTN_DEVINL int steps_of(int n, int t) { return (n - t + 1) / 2; }
@@ -187,10 +206,13 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.q_full[i], 1);
       mbar_init(&bars.q_empty[i], 2);          // both issuers, after their last QKᵀ of the tile
+      mbar_init(&bars.w_free[i], 2 * kBM);     // every softmax thread, once it has read the slot
     }
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);          // each stage is read by one issuer's MMAs
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
     }
@@ -230,57 +252,67 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
   // Register split, set inside each role: 128 x 80 (TMA, MMA, idle warps) +
   // 256 x 208 (softmax) <= 384 x 168 registers the CTA is launched with.
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // Warp 0: the tile's work description and Q, then its K tiles; warp 3:
+    // its V tiles. Apart, a V stage still held by an unfinished P̃V does not
+    // hold up the next K load.
     regs_dec<80>();
     if (lane == 0) {
       pdl_wait_primary();
-      tc::tma_prefetch_desc(&map_q);
-      tc::tma_prefetch_desc(&map_k);
-      tc::tma_prefetch_desc(&map_v);
-      int g = 0, issued_q = 0, issued_k = 0, issued_v = 0, k = 0;
+      const bool qk = warp == 0;
+      if (qk) {
+        tc::tma_prefetch_desc(&map_q);
+        tc::tma_prefetch_desc(&map_k);
+      } else {
+        tc::tma_prefetch_desc(&map_v);
+      }
+      int g = 0, issued_q = 0, issued = 0, k = 0;
       bool ok = true;
       for (int w = int(blockIdx.x); w < n_tiles && ok; w += int(gridDim.x), ++k) {
         const TileWork tw = tile_work(w);
-        // Q of tile k into buffer k % 2 once both issuers' QKᵀ of tile k - 2
-        // have read it
-        const int qs = k & 1;
-        ok = mbar_wait_bounded(&bars.q_empty[qs], ((k >> 1) & 1) ^ 1, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars.q_full[qs], kTileBytes);
-        tc::tma_load_3d(smem + kQOff + qs * kTileBytes, &map_q, 0, tw.row0, tw.bh,
-                        &bars.q_full[qs]);
-        ++issued_q;
+        if (qk) {
+          // Q of tile k into buffer k % 2 once both issuers' QKᵀ of tile k - 2
+          // have read it, its work into slot k % 2 once the softmax
+          // warpgroups have read tile k - 2's
+          const int qs = k & 1;
+          ok = mbar_wait_bounded(&bars.q_empty[qs], ((k >> 1) & 1) ^ 1, abort_flag);
+          if (ok) ok = mbar_wait_bounded(&bars.w_free[qs], ((k >> 1) & 1) ^ 1, abort_flag);
+          if (!ok) break;
+          bars.work[qs] = tw;
+          mbar_arrive_expect_tx(&bars.q_full[qs], kTileBytes);   // (releases the slot write)
+          tc::tma_load_3d(smem + kQOff + qs * kTileBytes, &map_q, 0, tw.row0, tw.bh,
+                          &bars.q_full[qs]);
+          ++issued_q;
+        }
+        const int stages = qk ? kKStages : kVStages;
+        uint64_t* full = qk ? bars.k_full : bars.v_full;
+        uint64_t* empty = qk ? bars.k_empty : bars.v_empty;
+        uint8_t* ring = smem + (qk ? kKOff : kVOff);
+        const CUtensorMap* map = qk ? &map_k : &map_v;
         for (int j = 0; j < tw.n; ++j, ++g) {
-          const int st = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
+          const int st = g % stages;
+          const uint32_t ph = (g / stages) & 1;
           const int key_tile = kGeneral ? tw.plan.tile(j) : j;
-          ok = mbar_wait_bounded(&bars.k_empty[st], ph ^ 1, abort_flag);
+          ok = mbar_wait_bounded(&empty[st], ph ^ 1, abort_flag);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars.k_full[st], kTileBytes);
-          tc::tma_load_3d(smem + kKOff + st * kTileBytes, &map_k, 0, key_tile * kBN, tw.kvh,
-                          &bars.k_full[st]);
-          ++issued_k;
-          ok = mbar_wait_bounded(&bars.v_empty[st], ph ^ 1, abort_flag);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bars.v_full[st], kTileBytes);
-          tc::tma_load_3d(smem + kVOff + st * kTileBytes, &map_v, 0, key_tile * kBN, tw.kvh,
-                          &bars.v_full[st]);
-          ++issued_v;
+          mbar_arrive_expect_tx(&full[st], kTileBytes);
+          tc::tma_load_3d(ring + st * kTileBytes, map, 0, key_tile * kBN, tw.kvh, &full[st]);
+          ++issued;
         }
       }
       if (!ok) {
         attn_flag_error(kErrTimeout);
         bars.abort = 1;
         // Drain: wait for the loads this thread issued that may still be in
-        // flight (the last two Q loads, the last kStages K and V loads) so
-        // no copy lands after the CTA exits.
+        // flight (the last two Q loads, the last ring's worth of K or V
+        // loads) so no copy lands after the CTA exits.
         for (int kq = max(0, issued_q - 2); kq < issued_q; ++kq)
           mbar_wait_bounded(&bars.q_full[kq & 1], (kq >> 1) & 1, nullptr);
-        for (int j = max(0, issued_k - kStages); j < issued_k; ++j)
-          mbar_wait_bounded(&bars.k_full[j % kStages], (j / kStages) & 1, nullptr);
-        for (int j = max(0, issued_v - kStages); j < issued_v; ++j)
-          mbar_wait_bounded(&bars.v_full[j % kStages], (j / kStages) & 1, nullptr);
+        const int stages = qk ? kKStages : kVStages;
+        uint64_t* full = qk ? bars.k_full : bars.v_full;
+        for (int j = max(0, issued - stages); j < issued; ++j)
+          mbar_wait_bounded(&full[j % stages], (j / stages) & 1, nullptr);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -303,39 +335,40 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
     int k = 0;
     bool any = false;
     for (int w = int(blockIdx.x); w < n_tiles && ok; w += int(gridDim.x), ++k) {
-      const TileWork tw = tile_work(w);
-      const int n = steps_of(tw.n, t);
       const int qs = k & 1;
       const uint32_t qa = q_base + qs * kTileBytes;
-      // step i reads load g0 + t + 2i; S_t(i) follows the softmax's read of
-      // this warpgroup's previous S
+      // Q of the tile and its work slot (both written before q_full)
+      ok = mbar_wait_warp(&bars.q_full[qs], (k >> 1) & 1, abort_flag);
+      if (!ok) break;
+      const TileWork tw = read_work(&bars.work[qs]);
+      const int n = steps_of(tw.n, t);
+      // step i reads load g0 + t + 2i of each ring; S_t(i) follows the
+      // softmax's read of this warpgroup's previous S
       auto issue_s = [&](int i) {
         const int g = g0 + t + 2 * i;
-        const uint32_t ka = k_base + (g % kStages) * kTileBytes;
+        const uint32_t ka = k_base + (g % kKStages) * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           tc::mma_ss_warp(tmem + col_s(t), tc::smem_desc(qa + kk * 32, 16, 1024, tc::kLayoutSW128),
                           tc::smem_desc(ka + kk * 32, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
         tc::mma_commit_warp(&bars.s_full[t]);
-        tc::mma_commit_warp(&bars.k_empty[g % kStages]);
+        tc::mma_commit_warp(&bars.k_empty[g % kKStages]);
         if (i == n - 1) tc::mma_commit_warp(&bars.q_empty[qs]);   // the tile's last read of Q
       };
       auto wait_s_inputs = [&](int i) {
         const int g = g0 + t + 2 * i;
         bool r = true;
         if (cs + i > 0) r = mbar_wait_warp(&bars.s_free[t], (cs + i - 1) & 1, abort_flag);
-        if (r) r = mbar_wait_warp(&bars.k_full[g % kStages], (g / kStages) & 1, abort_flag);
+        if (r) r = mbar_wait_warp(&bars.k_full[g % kKStages], (g / kKStages) & 1, abort_flag);
         return r;
       };
       if (n == 0) {
-        // nothing of this tile: release its Q buffer once loaded (each load
-        // completes one phase of q_full, each release one of q_empty)
-        ok = mbar_wait_warp(&bars.q_full[qs], (k >> 1) & 1, abort_flag);
-        if (ok && lane == 0) mbar_arrive(&bars.q_empty[qs]);
+        // nothing of this tile: release its Q buffer (each load completes
+        // one phase of q_full, each pair of releases one of q_empty)
+        if (lane == 0) mbar_arrive(&bars.q_empty[qs]);
         __syncwarp();
       } else {
-        ok = mbar_wait_warp(&bars.q_full[qs], (k >> 1) & 1, abort_flag);
-        if (ok) ok = wait_s_inputs(0);
+        ok = wait_s_inputs(0);
         if (ok) {
           tc::fence_after_sync();
           issue_s(0);
@@ -349,21 +382,21 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
             issue_s(i + 1);
           }
           const int g = g0 + t + 2 * i;
-          ok = mbar_wait_warp(&bars.v_full[g % kStages], (g / kStages) & 1, abort_flag);
+          ok = mbar_wait_warp(&bars.v_full[g % kVStages], (g / kVStages) & 1, abort_flag);
           if (ok) ok = mbar_wait_warp(&bars.p_full[t], (cs + i) & 1, abort_flag);
           // the first P̃V of a tile overwrites Õ_t: the previous tile's merge
           // has read it
           if (ok && i == 0) ok = mbar_wait_warp(&bars.o_free, (k & 1) ^ 1, abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
-          const uint32_t va = v_base + (g % kStages) * kTileBytes;
+          const uint32_t va = v_base + (g % kVStages) * kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             tc::mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
                             tc::smem_desc(va + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128),
                             idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit_warp(&bars.o_done[t]);
-          tc::mma_commit_warp(&bars.v_empty[g % kStages]);
+          tc::mma_commit_warp(&bars.v_empty[g % kVStages]);
         }
       }
       g0 += tw.n;
@@ -379,8 +412,6 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
       tc::mma_commit_warp(&bars.mma_drain[t]);
       mbar_wait_warp(&bars.mma_drain[t], 0, nullptr);
     }
-  } else if (warp < 4) {
-    regs_dec<80>();                                // idle warp of the first warpgroup
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     regs_inc<208>();
@@ -396,8 +427,12 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
     int cs = 0;                                    // this warpgroup's steps before the tile
     bool ok = true;
 
-    for (int w = int(blockIdx.x); w < n_tiles; w += int(gridDim.x)) {
-      const TileWork tw = tile_work(w);
+    for (int w = int(blockIdx.x), k = 0; w < n_tiles; w += int(gridDim.x), ++k) {
+      // the tile's work (written with its Q load into slot k % 2)
+      const int qs = k & 1;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.q_full[qs], (k >> 1) & 1, abort_flag));
+      const TileWork tw = read_work(&bars.work[qs]);
+      mbar_arrive(&bars.w_free[qs]);
       const int nt = steps_of(tw.n, t);
       const int row = tw.row0 + r;                 // query row
       const int b = tw.bh / Hq;
@@ -544,7 +579,7 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
         const float w0 = l0 > 0.f ? fast_exp2(m0 - mm) : 0.f;
         const float w1 = l1 > 0.f ? fast_exp2(m1 - mm) : 0.f;
         const float l = w0 * l0 + w1 * l1;
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
         const float a0 = w0 * inv_l, a1 = w1 * inv_l;
         uint32_t pk[16];
 #pragma unroll
