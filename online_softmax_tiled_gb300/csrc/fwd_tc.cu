@@ -1,5 +1,6 @@
-// bf16 tiled attention forward on the sm_103a tensor cores (tcgen05 + TMEM +
-// TMA).
+// bf16 tiled attention forward at head dimension 128 on the sm_103a tensor
+// cores (tcgen05 + TMEM + TMA); d = 64 runs the persistent kernel of
+// fwd_tc64.cu.
 //
 // Algorithm: the inner loop of the "Flash Attention 2" post
 // (ahmadsaeedzaidi.github.io feed), section "Flash Attention 2": for a query
@@ -51,7 +52,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: Õ is rescaled when m 
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static_assert(D == 128, "d = 64 runs fwd_tc64_kernel");
+  static constexpr int kStages = 2;
   static constexpr int kAtoms = D / 64;                   // 128-byte swizzle atoms per row
   static constexpr int kTileBytes = kBM * D * 2;          // Q, K or V tile
   static constexpr int kQOff = 0;                         // Q0, Q1
@@ -59,22 +61,17 @@ struct FwdCfg {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kVOff + kStages * kTileBytes;
   static constexpr int kDynSmem = kSmemBytes + 1024;      // slack for 1024-byte alignment
-  // TMEM columns. d = 128: S0, S1, O0, O1 fill all 512 columns and P̃ is
-  // written over the scores it came from. d = 64: 128 columns are left, so
-  // each tile's P̃ gets its own 64 columns; the next S can then be computed
-  // as soon as the softmax has read the current one.
-  static constexpr bool kSeparateP = (D == 64);
+  // TMEM columns: S0, S1, O0, O1 fill all 512 columns and P̃ is written over
+  // the scores it came from.
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
-  static constexpr uint32_t kColP0 = kSeparateP ? 256 + 2 * D : kColS0;
-  static constexpr uint32_t kColP1 = kSeparateP ? 256 + 2 * D + 64 : kColS1;
-  static_assert(!kSeparateP || kColP1 + 64 <= 512, "TMEM budget");
+  static constexpr uint32_t kColP0 = kColS0, kColP1 = kColS1;
 };
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
-  uint64_t mma_drain[2];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t mma_drain;
   uint32_t tmem_base;
   int abort;
   PlanSlots plan;   // keys the CTA's rows see (general masks)
@@ -127,10 +124,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               float* __restrict__ lse, int Hq, int Hkv, int Nq, int Nk, float scale,
               MaskSpec mask, int n_qblk, int order_grp) {
   using C = FwdCfg<D>;
-  // d = 64: one MMA-issuing thread per query tile (each waits only on its own
-  // tile). d = 128 (P̃ over the scores): one thread in the interleaved order
-  // S0, S1, PV0, S0', PV1, S1', ... measured faster there.
-  constexpr int kIssuers = C::kSeparateP ? 2 : 1;
   // Launched as a programmatic dependent of whatever precedes it in the
   // stream: the prologue (barriers, TMEM) overlaps that kernel's tail and
   // the TMA producer waits for it before the first load. Every global access
@@ -158,18 +151,16 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     mbar_init(&bars.q_full, 1);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars.k_full[i], 1);
-      mbar_init(&bars.k_empty[i], kIssuers);   // one release per MMA-issuing thread
+      mbar_init(&bars.k_empty[i], 1);
       mbar_init(&bars.v_full[i], 1);
-      mbar_init(&bars.v_empty[i], kIssuers);
+      mbar_init(&bars.v_empty[i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.s_free[t], kBM);
       mbar_init(&bars.p_full[t], kBM);
       mbar_init(&bars.o_done[t], 1);
     }
-    mbar_init(&bars.mma_drain[0], 1);
-    mbar_init(&bars.mma_drain[1], 1);
+    mbar_init(&bars.mma_drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -269,102 +260,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
           mbar_wait_bounded(&bars.v_full[j % C::kStages], (j / C::kStages) & 1, nullptr);
       }
     }
-  } else if (C::kSeparateP && (warp == 1 || warp == 2)) {
-    // ------------------------------------------------------------ MMA issuers (d = 64)
-    // One issuing warp per query tile (each runs its loop converged; one
-    // elected lane issues). tcgen05.mma issue only returns as the tensor pipe
-    // accepts the instruction (its queue is shallow), so a single issuer
-    // waiting on one tile's barrier would starve the pipe even when the other
-    // tile's work is ready.
-    regs_dec<80>();
-    const int t = warp - 1;
-    const int n = n_t[t], n_other = n_t[t ^ 1];
-    if (nj > 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kBM, D, false, true);
-      const uint32_t s_col = t == 0 ? C::kColS0 : C::kColS1;
-      const uint32_t o_col = t == 0 ? C::kColO0 : C::kColO1;
-      const uint32_t p_col = t == 0 ? C::kColP0 : C::kColP1;
-      const uint32_t qa = smem_u32(smem + C::kQOff) + t * C::kTileBytes;
-      const uint32_t k_base = smem_u32(smem + C::kKOff);
-      const uint32_t v_base = smem_u32(smem + C::kVOff);
-
-      // K_j / V_j stages are released by both threads (count 2); where the
-      // other tile does not visit index j this thread releases twice (the
-      // plain arrival, the commit only once its MMAs have read the stage).
-      auto release = [&](uint64_t* bar, int j) {
-        tc::mma_commit_warp(bar);
-        if (j >= n_other && lane == 0) mbar_arrive(bar);
-        __syncwarp();
-      };
-      auto issue_s = [&](int j) {
-        const uint32_t ka = k_base + (j % C::kStages) * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (kBM * 128) + (kk % 4) * 32;
-          tc::mma_ss_warp(tmem + s_col, tc::smem_desc(qa + off, 16, 1024, tc::kLayoutSW128),
-                          tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSW128), idesc_s, kk > 0);
-        }
-        tc::mma_commit_warp(&bars.s_full[t]);
-        release(&bars.k_empty[j % C::kStages], j);
-      };
-      auto issue_pv = [&](int j) {
-        const uint32_t va = v_base + (j % C::kStages) * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          tc::mma_ts_warp(tmem + o_col, tmem + p_col + kk * 8,
-                          tc::smem_desc(va + kk * 2048, kBN * 128, 1024, tc::kLayoutSW128), idesc_o,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc::mma_commit_warp(&bars.o_done[t]);
-        release(&bars.v_empty[j % C::kStages], j);
-      };
-
-      bool ok = true;
-      if (n > 0) {
-        ok = mbar_wait_warp(&bars.q_full, 0, abort_flag);
-        if (ok) ok = mbar_wait_warp(&bars.k_full[0], 0, abort_flag);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_s(0);
-        }
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        const int j1 = j + 1;
-        if (C::kSeparateP && j1 < n) {
-          // S_t(j+1) as soon as the softmax has read S_t(j) and K_{j+1} is in
-          ok = mbar_wait_warp(&bars.s_free[t], j & 1, abort_flag);
-          if (ok) ok = mbar_wait_warp(&bars.k_full[j1 % C::kStages], (j1 / C::kStages) & 1,
-                                      abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_s(j1);
-        }
-        ok = mbar_wait_warp(&bars.v_full[j % C::kStages], (j / C::kStages) & 1, abort_flag);
-        if (ok) ok = mbar_wait_warp(&bars.p_full[t], j & 1, abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        issue_pv(j);
-        if (!C::kSeparateP && j1 < n) {
-          // P̃_t(j) lives in the S_t columns: S_t(j+1) after PV_t(j) (issue order)
-          ok = mbar_wait_warp(&bars.k_full[j1 % C::kStages], (j1 / C::kStages) & 1, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_s(j1);
-        }
-      }
-      if (!ok && lane == 0) {
-        attn_flag_error(kErrTimeout);
-        bars.abort = 1;
-      }
-      __syncwarp();
-      // Drain: every MMA this warp issued has completed before TMEM is freed.
-      tc::mma_commit_warp(&bars.mma_drain[t]);
-      mbar_wait_warp(&bars.mma_drain[t], 0, nullptr);
-    }
-  } else if (!C::kSeparateP && warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (d = 128)
-    // The whole warp runs this loop; one elected lane issues each MMA.
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop; one elected lane issues each MMA, in the
+    // order S0, S1, PV0, S0', PV1, S1', ... (P̃ lives in the S columns, so
+    // S_t(j+1) follows PV_t(j)).
     regs_dec<80>();
     if (nj > 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kBM, kBN, false, false);
@@ -430,8 +330,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       __syncwarp();
       // Drain: every MMA this warp issued has completed before TMEM is freed.
-      tc::mma_commit_warp(&bars.mma_drain[0]);
-      mbar_wait_warp(&bars.mma_drain[0], 0, nullptr);
+      tc::mma_commit_warp(&bars.mma_drain);
+      mbar_wait_warp(&bars.mma_drain, 0, nullptr);
     }
   } else if (warp < 4) {
     regs_dec<80>();                                // idle warp of the first warpgroup
@@ -471,10 +371,6 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       tc::tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
       tc::tmem_ld_wait();
       float* s = reinterpret_cast<float*>(sr);
-      if (C::kSeparateP) {            // S_t may be recomputed for the next tile now
-        tc::fence_before_sync();
-        mbar_arrive(&bars.s_free[t]);
-      }
 
       // Mask the keys this row does not see (past the end included) in a
       // tile that straddles one of its bounds.
@@ -513,46 +409,21 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
-      // P̃ = exp2(s·c - m_ref) -> bf16 pairs (over the first 64 score columns,
-      // or into the tile's own P̃ columns).
+      // P̃ = exp2(s·c - m_ref) -> bf16 pairs over the first 64 score columns
       const f2 cc2{c, c}, nm2{neg_m, neg_m};
       f2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // 4 independent sums
-      bool pv_prev_done = false;
-      if (C::kSeparateP) {
-        // With its own P̃ columns, P̃_t(j) may only be written once PV_t(j-1)
-        // has read P̃_t(j-1): all 128 exponentials are computed first, so the
-        // wait overlaps the special-function work instead of preceding it.
-        uint32_t pk[64];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          f2 x = fma2(f2{s[2 * e], s[2 * e + 1]}, cc2, nm2);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          f2 x = fma2(f2{s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]}, cc2, nm2);
           x.x = fast_exp2(x.x);
           x.y = fast_exp2(x.y);
           rs2[e & 3] = add2(rs2[e & 3], x);
           pk[e] = pack_bf16x2(x.x, x.y);
         }
-        if (j > 0) {   // the same wait covers the Õ rescale below
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.o_done[t], (j - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc::fence_after_sync();
-          pv_prev_done = true;
-        }
-        tmem_st32(p_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(p_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      } else {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            f2 x = fma2(f2{s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]}, cc2, nm2);
-            x.x = fast_exp2(x.x);
-            x.y = fast_exp2(x.y);
-            rs2[e & 3] = add2(rs2[e & 3], x);
-            pk[e] = pack_bf16x2(x.x, x.y);
-          }
-          tmem_st32(p_addr + half * 32, pk);
-        }
+        tmem_st32(p_addr + half * 32, pk);
       }
       const f2 rsa = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
       const float rs = rsa.x + rsa.y;
@@ -560,11 +431,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 
       // Rescale Õ (once the previous P̃V has landed) when the reference moved.
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        if (!pv_prev_done) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.o_done[t], (j - 1) & 1, abort_flag));
-          if (!ok) break;
-          tc::fence_after_sync();
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.o_done[t], (j - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t orr[32];
@@ -676,8 +545,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
   const MaskSpec& m = a.mask;
   const bool plain = m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
                      m.row_kv_start == nullptr;   // no mask, or causal
-  if (plain) return a.d == 64 ? launch_fwd_tc_d<64, false>(a) : launch_fwd_tc_d<128, false>(a);
-  return a.d == 64 ? launch_fwd_tc_d<64, true>(a) : launch_fwd_tc_d<128, true>(a);
+  return plain ? launch_fwd_tc_d<128, false>(a) : launch_fwd_tc_d<128, true>(a);
 }
 
 }  // namespace attn
