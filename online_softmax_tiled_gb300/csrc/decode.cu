@@ -19,7 +19,8 @@
 // `sub` holds dims {64v + 8sub .. 64v + 8sub + 7}, so a warp's 16-byte
 // shared loads cover whole 128-byte rows without bank conflicts. Each 8-lane
 // group runs its own online softmax over its keys; the 16 groups of the CTA
-// are merged with the same exact rule at the end.
+// are merged with the same exact rule at the end (the four groups of a warp
+// by shuffles, then the four warps through shared memory).
 //
 // Paged, variable-length decode (ML notes, KV-cache Q&A: the cache lives in
 // fixed-size blocks reached through a per-request block table, as pages
@@ -55,12 +56,93 @@ constexpr int kChunkPagesCached = 256;   // block-table entries of a chunk kept 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// End of a chunk, shared by both split kernels so that they round alike.
+// Each 8-lane group holds (m, l, o) relative to its own reference. The four
+// groups of a warp (lanes 8 apart hold the same dimensions) are first
+// rescaled onto their common max and summed with shuffles; lanes 0..7 then
+// write the warp's (o, m, l) to comb[warp][h][0 .. D + 1]. NP = D / 16
+// dimension pairs per lane, NV = D / 64 16-byte pieces.
+template <int D, int G>
+ATTN_DEVINL void warp_combine_write(f2 (&acc)[G][D / 16], float (&m_ref)[G], float (&l_run)[G],
+                                    float* comb, int warp, int lane) {
+  constexpr int NP = D / 16, NV = D / 64;
+  const int grp = lane >> 3, sub = lane & 7;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float mw = fmaxf(m_ref[h], __shfl_xor_sync(0xffffffffu, m_ref[h], 8));
+    mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+    const float wgt = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(m_ref[h] - mw);
+    float l = l_run[h] * wgt;
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    l_run[h] = l;
+    m_ref[h] = mw;
+    const f2 w2{wgt, wgt};
+#pragma unroll
+    for (int e = 0; e < NP; ++e) {
+      f2 a = mul2(acc[h][e], w2);
+      a.x += __shfl_xor_sync(0xffffffffu, a.x, 8);
+      a.y += __shfl_xor_sync(0xffffffffu, a.y, 8);
+      a.x += __shfl_xor_sync(0xffffffffu, a.x, 16);
+      a.y += __shfl_xor_sync(0xffffffffu, a.y, 16);
+      acc[h][e] = a;
+    }
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float* row = comb + (warp * G + h) * (D + 2);
+      if (sub == 0) {
+        row[D] = m_ref[h];
+        row[D + 1] = l_run[h];
+      }
+#pragma unroll
+      for (int vv = 0; vv < NV; ++vv)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          row[64 * vv + 8 * sub + 2 * e] = acc[h][vv * 4 + e].x;
+          row[64 * vv + 8 * sub + 2 * e + 1] = acc[h][vv * 4 + e].y;
+        }
+    }
+  }
+}
+
+// The four warps' (o, m, l) of each query row onto their common max: the
+// chunk's partial o (un-normalised), m (natural units) and l, written for
+// rows row0 .. row0 + G - 1 at split s. Threads tid, tid + nthr, ...
+template <int D, int G>
+ATTN_DEVINL void final_combine(const float* comb, int tid, int nthr, size_t row0, int S, int s,
+                               float* o_part, float* m_part, float* l_part) {
+  for (int idx = tid; idx < G * D; idx += nthr) {
+    const int h = idx / D, c = idx % D;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, comb[(w * G + h) * (D + 2) + D]);
+    float o = 0.f, l = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float* row = comb + (w * G + h) * (D + 2);
+        const float wt = (row[D] == -INFINITY) ? 0.f : fast_exp2(row[D] - mx);
+        o = fmaf(wt, row[c], o);
+        l = fmaf(wt, row[D + 1], l);
+      }
+    }
+    const size_t qrow = row0 + h;
+    o_part[(qrow * S + s) * D + c] = o;
+    if (c == 0) {
+      m_part[qrow * S + s] = (mx == -INFINITY) ? -INFINITY : mx * kLn2;   // natural units
+      l_part[qrow * S + s] = l;
+    }
+  }
+}
+
 template <int D, int G>
 constexpr size_t decode_smem_bytes() {
-  // K and V ring; the final cross-group merge (16 groups × G heads of
-  // (m, l, o[D]) in float32) reuses it.
+  // K and V ring; the final cross-warp combine (4 warps × G heads of
+  // (o[D], m, l) in float32) reuses it.
   constexpr size_t ring = size_t(2) * kStages * kStageKeys * D * 2;
-  constexpr size_t merge = size_t(16) * G * (D + 2) * 4;
+  constexpr size_t merge = size_t(4) * G * (D + 2) * 4;
   return ring > merge ? ring : merge;
 }
 
@@ -365,53 +447,13 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   }
   if (!ok) return;
 
-  // Cross-group merge: 16 groups × G heads, exact rescale onto the common max.
+  // Cross-group merge: exact rescale onto the common max, first the four
+  // groups of each warp, then the four warps.
+  __syncthreads();   // every warp is done with the ring, which the combine reuses
+  float* comb = reinterpret_cast<float*>(smem);
+  warp_combine_write<D, G>(acc, m_ref, l_run, comb, warp, lane);
   __syncthreads();
-  float* sm_m = reinterpret_cast<float*>(smem);                 // [16][G]
-  float* sm_l = sm_m + 16 * G;                                  // [16][G]
-  float* sm_o = sm_l + 16 * G;                                  // [16][G][D]
-  const int gid = warp * 4 + grp;
-  if (sub == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      sm_m[gid * G + h] = m_ref[h];
-      sm_l[gid * G + h] = l_run[h];
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int vv = 0; vv < NV; ++vv)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float* dst = sm_o + (gid * G + h) * D + 64 * vv + 8 * sub + 2 * e;
-        dst[0] = acc[h][vv * 4 + e].x;
-        dst[1] = acc[h][vv * 4 + e].y;
-      }
-  __syncthreads();
-
-  for (int idx = tid; idx < G * D; idx += kThreads) {
-    const int h = idx / D, c = idx % D;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < 16; ++t) mx = fmaxf(mx, sm_m[t * G + h]);
-    float o = 0.f, l = 0.f;
-    if (mx != -INFINITY) {
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float mt = sm_m[t * G + h];
-        const float w = (mt == -INFINITY) ? 0.f : fast_exp2(mt - mx);
-        o = fmaf(w, sm_o[(t * G + h) * D + c], o);
-        l = fmaf(w, sm_l[t * G + h], l);
-      }
-    }
-    const size_t row = size_t(b) * Hq + gy * G + h;
-    o_part[(row * S + s) * D + c] = o;
-    if (c == 0) {
-      m_part[row * S + s] = (mx == -INFINITY) ? -INFINITY : mx * kLn2;  // back to natural units
-      l_part[row * S + s] = l;
-    }
-  }
+  final_combine<D, G>(comb, tid, kThreads, size_t(b) * Hq + gy * G, S, s, o_part, m_part, l_part);
 }
 
 // One warp per output row; lane owns float4 column groups lane, lane+32, ...
