@@ -87,6 +87,14 @@ def test_lse_optional(ost):
     assert np.max(np.abs(to_f64(o) - o_ref)) <= 2e-2
 
 
+def test_d64_causal_several_tiles_per_cta(ost):
+    """d = 64 causal with more 128-row query tiles (384) than SMs: a CTA of
+    the persistent forward runs two or three tiles with different key-tile
+    counts, ragged tail, every output element."""
+    _check_full(ost, Workload("causal_many", "fwd", 2, 16, 8, 1500, 1500, 64, "bf16", True,
+                              seed=41))
+
+
 def test_mha_workload_full(ost):
     """B=4, H=16, N=2048, d=64 bf16, every output element."""
     _check_full(ost, WORKLOADS["fwd_mha_n2048_d64"])

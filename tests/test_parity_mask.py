@@ -63,6 +63,14 @@ def test_window_and_global_masks(ost, dtype, d, name):
     _check(ost, w, SPECS[name])
 
 
+def test_window_d64_several_tiles_per_cta(ost):
+    """A sliding window with sinks at d = 64 over 384 query tiles: each CTA
+    of the persistent forward plans two or three tiles, each its own key
+    tile ranges."""
+    w = Workload("mask_many", "fwd", 2, 16, 8, 1500, 1500, 64, "bf16", seed=43)
+    _check(ost, w, {"window_left": 200, "window_right": 0, "n_global": 5})
+
+
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 64)])
 @pytest.mark.parametrize("causal", [True, False])
 def test_document_masks(ost, dtype, d, causal):
