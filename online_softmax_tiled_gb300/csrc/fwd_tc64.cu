@@ -7,9 +7,11 @@
 // row max m, P̃ = exp(S - m), running denominator l, Õ rescaled by
 // exp(m_old - m_new) and accumulated with P̃ V_j; after the last tile
 // O_i = Õ_i / l_i and LSE = m + ln l. Masks per the post's section "Causal
-// masking", option A (mask.cuh). The post also notes that the partial
-// results of disjoint key ranges combine exactly by rescaling onto the
-// larger max; that is how the two halves of a query tile's keys meet here.
+// masking", option A (mask.cuh). The two halves of a query tile's keys meet
+// by the exact partition merge of the attention-residuals kernel lab
+// (manishklach.github.io, "Phase 2") and the split-K notes of the ML notes
+// (haolingpu.github.io): each partial result is rescaled onto the larger
+// max and the sums are added.
 //
 // GB300 mapping at d = 64 (fwd_tc.cu keeps d = 128):
 //  * At d = 64 a 128 x 128 step is short (about 1.2 us), so a one-tile CTA
@@ -17,7 +19,9 @@
 //    first Q and K loads) and draining (the last P̃V, the store). One CTA per
 //    SM instead loops over 128-row query tiles (static round robin over the
 //    grid), and its producer and MMA warps run into the next tile while the
-//    softmax warps finish the current one.
+//    softmax warps finish the current one. Warp 0 writes each tile's work
+//    (coordinates and key-tile plan) into a shared slot and loads its Q and
+//    K tiles; warp 3 loads the V tiles.
 //  * The CTA's two softmax warpgroups split the key tiles of a query tile:
 //    warpgroup t takes plan indices t, t + 2, ... with its own S_t, P̃_t and
 //    Õ_t in tensor memory, its own (m, l) in registers, and its own MMA
@@ -26,8 +30,9 @@
 //  * TMEM: S0, S1 (128 columns each), Õ0, Õ1 (64 each), P̃0, P̃1 (64 each,
 //    bf16 pairs): the next S_t is computed as soon as the softmax has read
 //    the current one.
-//  * Shared memory: two Q buffers (the next tile's Q loads early), a 4-stage
-//    K/V ring indexed by a load counter that runs across tiles, and an O
+//  * Shared memory: two Q buffers (the next tile's Q loads early), K and V
+//    rings of 6 and 4 stages indexed by load counters that run across tiles
+//    (a K stage frees after its QKᵀ, a V stage only after its P̃V), and an O
 //    staging tile for the TMA store.
 //  * Every mbarrier wait is bounded; a timeout sets the error word, raises a
 //    CTA abort flag and every role drains its in-flight work before exit.
@@ -249,7 +254,7 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
     __syncthreads();
   }
 
-  // Register split, set inside each role: 128 x 80 (TMA, MMA, idle warps) +
+  // Register split, set inside each role: 128 x 80 (the TMA and MMA warps) +
   // 256 x 208 (softmax) <= 384 x 168 registers the CTA is launched with.
 
   if (warp == 0 || warp == 3) {
