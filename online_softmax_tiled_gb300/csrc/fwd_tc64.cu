@@ -431,6 +431,11 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
     const bool storer = warp == 4 && lane == 0;    // issues the tile's TMA store
     int cs = 0;                                    // this warpgroup's steps before the tile
     bool ok = true;
+    // An mbarrier probe takes ~150 cycles to answer even when the phase is
+    // long complete, so the next step's S-full and this step's P̃V-done are
+    // probed early without blocking (test_wait) and the answers used later;
+    // a phase not yet complete then is waited for as usual.
+    bool s_ready = false;                          // S of the next step known complete
 
     for (int w = int(blockIdx.x), k = 0; w < n_tiles; w += int(gridDim.x), ++k) {
       // the tile's work (written with its Q load into slot k % 2)
@@ -452,10 +457,12 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
       for (int i = 0; i < nt && ok; ++i) {
         const int ci = cs + i;
         // Waits are made warp-uniform: tcgen05.ld/st below are warp-collective.
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars.s_full[t], ci & 1, abort_flag))) {
+        if (!__all_sync(0xffffffffu,
+                        s_ready || mbar_wait_bounded(&bars.s_full[t], ci & 1, abort_flag))) {
           ok = false;
           break;
         }
+        s_ready = false;
         tc::fence_after_sync();
         uint32_t sr[128];
         tc::tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -504,6 +511,7 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
           m_ref = m_cand;
         }
         const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const bool pv_ready = i > 0 && mbar_test_wait(&bars.o_done[t], (ci - 1) & 1);
 
         // P̃ = exp2(s·c - m_ref) -> bf16 pairs, all 128 first: P̃_t may only
         // be written once the previous P̃V of this warpgroup has read it, and
@@ -519,10 +527,13 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
           rs2[e & 3] = add2(rs2[e & 3], x);
           pk[e] = pack_bf16x2(x.x, x.y);
         }
+        // the next step's scores (the following tile's first, after the last)
+        const bool s_next = mbar_test_wait(&bars.s_full[t], (ci + 1) & 1);
         // (the previous P̃V of this warpgroup in an earlier tile was waited
         // for by that tile's merge)
         if (i > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars.o_done[t], (ci - 1) & 1, abort_flag));
+          ok = __all_sync(0xffffffffu, pv_ready ||
+                                       mbar_wait_bounded(&bars.o_done[t], (ci - 1) & 1, abort_flag));
           if (!ok) break;
           tc::fence_after_sync();
         }
@@ -546,6 +557,7 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::tmem_st_wait();
         tc::fence_before_sync();
         mbar_arrive(&bars.p_full[t]);
+        s_ready = __all_sync(0xffffffffu, s_next);
       }
       cs += nt;
 
