@@ -1,14 +1,21 @@
 """Benchmark of the tiled-attention hot path on GB300.
 
-Default workload (N=1): the batched multi-head forward B=4, H=16, N=2048,
-d=64, bf16, non-causal. ``--workload`` selects the other workloads
-(fwd_causal_n8192_d128, bwd_causal_n4096_d128, decode_gqa_l4096,
-decode_paged_gqa_l4096, fwd_f32_single_head). A step is one pass of the workload's hot path through
-the C ABI on inputs already resident in HBM; L2 is flushed (256 MiB write)
+Default run (N=1): the long-context causal forward B=2, H=32, N=8192, d=128,
+bf16 (the line's top-level value), followed in the same process by the
+causal backward B=2, H=16, N=4096, d=128, the GQA split-KV decode (B=64,
+Hq=32, Hkv=8, L=4096, 16 splits) and the batched multi-head forward B=4,
+H=16, N=2048, d=64, each reported under ``workloads`` with its own value,
+roofline, CPU baseline, end-to-end rate and clocks. ``--workload`` picks the
+top-level workload and ``--extra`` the others (``--extra none``: only the
+top-level one). A step is one pass of the workload's hot path through the C
+ABI on inputs already resident in HBM; L2 is flushed (256 MiB write)
 between timed steps unless the inputs exceed L2.
 
-Prints ONE JSON line (rank 0). ``--impl reference`` times the float64 CPU
-oracle as the reference arm instead.
+Before a workload is timed, one step's outputs are compared with the float64
+oracle on the heads (or requests) that the CPU-baseline leg computes, at the
+tolerances of the benchmark description; a mismatch ends the run with no
+line. Prints ONE JSON line (rank 0). ``--impl reference`` times the float64
+CPU oracle as the reference arm instead.
 
 Multi-GPU: every rank runs an independent replica of the workload (the path
 shards over batch and heads with no exchange), so value = N x units / max
@@ -219,15 +226,70 @@ class ClockSampler:
 
 # ----------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(w, inputs, budget_s: float):
-    """Time the float64 oracle on whole (b, h) heads of the workload until the
-    budget is spent; returns (units processed, seconds, description)."""
+class ParityTally:
+    """Largest |GPU - oracle| and |oracle| per output over the sampled units.
+    Where both sides are -inf (a row with no visible key: LSE), the error is 0."""
+
+    def __init__(self, outs):
+        self.outs = outs          # name -> float64 host array of the GPU result, or None
+        self.err = {}
+        self.ref = {}
+
+    def add(self, name, got, ref):
+        import numpy as np
+        if self.outs is None or name not in self.outs:
+            return
+        got = np.asarray(got, dtype=np.float64)
+        ref = np.asarray(ref, dtype=np.float64)
+        both_inf = np.isneginf(got) & np.isneginf(ref)
+        with np.errstate(invalid="ignore"):
+            diff = np.where(both_inf, 0.0, np.abs(got - ref))
+        fin = np.where(np.isfinite(ref), np.abs(ref), 0.0)
+        e = float(np.max(diff)) if diff.size else 0.0
+        r = float(np.max(fin)) if fin.size else 0.0
+        if np.isnan(e):
+            e = float("inf")
+        self.err[name] = max(self.err.get(name, 0.0), e)
+        self.ref[name] = max(self.ref.get(name, 0.0), r)
+
+    def report(self):
+        return {n: {"max_abs_err": self.err[n], "max_abs_ref": self.ref[n],
+                    "rel": self.err[n] / self.ref[n] if self.ref[n] > 0 else None}
+                for n in sorted(self.err)}
+
+
+def parity_failures(w, report):
+    """The outputs whose error exceeds the benchmark description's tolerance:
+    float32 inputs max|err| <= 1e-5; bf16 O <= 2e-2, LSE <= 1e-3, gradients
+    <= 5e-2 * max|ref|."""
+    bad = []
+    for name, r in report.items():
+        if w.dtype == "f32":
+            tol = 1e-5
+        elif name == "lse":
+            tol = 1e-3
+        elif name in ("dq", "dk", "dv"):
+            tol = 5e-2 * r["max_abs_ref"]
+        else:
+            tol = 2e-2
+        if not r["max_abs_err"] <= tol:
+            bad.append(f"{name}: max|err| {r['max_abs_err']:.3e} > {tol:.3e}")
+    return bad
+
+
+def cpu_oracle_sample(w, inputs, budget_s: float, gpu_outs=None):
+    """Time the float64 oracle on whole (b, h) heads (decode: whole requests)
+    of the workload until the budget is spent. When ``gpu_outs`` (name ->
+    float64 host array of one GPU step's outputs) is given, every sampled
+    unit is also compared with it. Returns (units processed, seconds,
+    description, ParityTally)."""
     import numpy as np
     import torch
 
     import oracle
     from workloads import to_f64
 
+    tally = ParityTally(gpu_outs)
     units_total, _, _ = algorithmic_units(w, inputs)
     t0 = time.perf_counter()
     done = 0
@@ -236,14 +298,18 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
         idx = inputs["indices"].numpy()
         units = 0
         for b in range(w.B):
-            oracle.decode_sparse(to_f64(inputs["q"][b:b + 1]), to_f64(inputs["k"][b:b + 1]),
-                                 to_f64(inputs["v"][b:b + 1]), idx[b:b + 1], cnt[b:b + 1],
-                                 w.scale)
+            o_r, l_r = oracle.decode_sparse(to_f64(inputs["q"][b:b + 1]),
+                                            to_f64(inputs["k"][b:b + 1]),
+                                            to_f64(inputs["v"][b:b + 1]), idx[b:b + 1],
+                                            cnt[b:b + 1], w.scale)
+            if gpu_outs is not None:
+                tally.add("o", gpu_outs["o"][b:b + 1], o_r)
+                tally.add("lse", gpu_outs["lse"][b:b + 1], l_r)
             units += sparse_bytes(w, cnt[b:b + 1].tolist())
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
-        return units, time.perf_counter() - t0, f"{done} of {w.B} requests"
+        return units, time.perf_counter() - t0, f"{done} of {w.B} requests", tally
     if w.kind == "decode_paged":
         lens = inputs["seq_lens"].numpy()
         table = inputs["block_table"].numpy()
@@ -255,35 +321,50 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
             idx = torch.as_tensor(pages.astype("int64"))
             k, v = to_f64(kp[idx]), to_f64(vp[idx])
             local = np.arange(len(pages), dtype=np.int32)[None, :]
-            oracle.decode_paged(to_f64(inputs["q"][b:b + 1]), k, v, local, lens[b:b + 1],
-                                w.page_size, w.scale)
+            o_r, l_r = oracle.decode_paged(to_f64(inputs["q"][b:b + 1]), k, v, local,
+                                           lens[b:b + 1], w.page_size, w.scale)
+            if gpu_outs is not None:
+                tally.add("o", gpu_outs["o"][b:b + 1], o_r)
+                tally.add("lse", gpu_outs["lse"][b:b + 1], l_r)
             units += paged_bytes(w, lens[b:b + 1].tolist())
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
-        return units, time.perf_counter() - t0, f"{done} of {w.B} requests"
+        return units, time.perf_counter() - t0, f"{done} of {w.B} requests", tally
     if w.kind == "decode":
         per_req = units_total / w.B
         for b in range(w.B):
             q = to_f64(inputs["q"][b:b + 1])
             k, v = to_f64(inputs["k"][b:b + 1]), to_f64(inputs["v"][b:b + 1])
-            oracle.decode_splitkv(q, k, v, w.scale, w.num_splits)
+            o_r, l_r = oracle.decode_splitkv(q, k, v, w.scale, w.num_splits)
+            if gpu_outs is not None:
+                tally.add("o", gpu_outs["o"][b:b + 1], o_r)
+                tally.add("lse", gpu_outs["lse"][b:b + 1], l_r)
             done += 1
             if time.perf_counter() - t0 > budget_s:
                 break
-        return per_req * done, time.perf_counter() - t0, f"{done} of {w.B} requests"
-    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+        return per_req * done, time.perf_counter() - t0, f"{done} of {w.B} requests", tally
+    # Heads taken alternately from both ends of the (b, h) order, so that a
+    # short budget still samples the first and the last batch entry and head.
+    flat = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    heads = [flat[i // 2] if i % 2 == 0 else flat[-1 - i // 2] for i in range(len(flat))]
     per_head = units_total / len(heads)
     r = w.Hq // w.Hkv
     done_units = 0.0
     for b, h in heads:
         sl = lambda t, hh: to_f64(t[b:b + 1, hh:hh + 1])
         q, k, v = sl(inputs["q"], h), sl(inputs["k"], h // r), sl(inputs["v"], h // r)
-        if w.kind == "bwd" and w.masked:
-            oracle.attention_bwd_masked(q, k, v, sl(inputs["do"], h), w.scale, mask_spec(w, inputs))
-            done_units += per_head
-        elif w.kind == "bwd":
-            oracle.attention_bwd(q, k, v, sl(inputs["do"], h), w.scale, w.causal)
+        if w.kind == "bwd":
+            if w.masked:
+                ref = oracle.attention_bwd_masked(q, k, v, sl(inputs["do"], h), w.scale,
+                                                  mask_spec(w, inputs))
+            else:
+                ref = oracle.attention_bwd(q, k, v, sl(inputs["do"], h), w.scale, w.causal)
+            if gpu_outs is not None:
+                tally.add("dq", gpu_outs["dq"][b:b + 1, h:h + 1], ref[0])
+                if r == 1:  # with GQA a KV head's dK, dV sum over its group
+                    tally.add("dk", gpu_outs["dk"][b:b + 1, h:h + 1], ref[1])
+                    tally.add("dv", gpu_outs["dv"][b:b + 1, h:h + 1], ref[2])
             done_units += per_head
         elif w.masked:
             spec = mask_spec(w, inputs)
@@ -292,16 +373,19 @@ def cpu_oracle_sample(w, inputs, budget_s: float):
                 if key in spec:
                     spec[key] = spec[key][b:b + 1]
                     xb[key] = inputs[key][b:b + 1]
-            oracle.attention_fwd_masked(q, k, v, w.scale, spec)
+            o_r, l_r = oracle.attention_fwd_masked(q, k, v, w.scale, spec)
             done_units += 4.0 * w.d * visible_pairs(
                 dataclasses.replace(w, B=1), xb) if xb else units_total / len(heads)
         else:
-            oracle.attention_fwd(q, k, v, w.scale, w.causal)
+            o_r, l_r = oracle.attention_fwd(q, k, v, w.scale, w.causal)
             done_units += per_head
+        if w.kind == "fwd" and gpu_outs is not None:
+            tally.add("o", gpu_outs["o"][b:b + 1, h:h + 1], o_r)
+            tally.add("lse", gpu_outs["lse"][b:b + 1, h:h + 1], l_r)
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    return done_units, time.perf_counter() - t0, f"{done} of {len(heads)} heads (b, h)"
+    return done_units, time.perf_counter() - t0, f"{done} of {len(heads)} heads (b, h)", tally
 
 
 def input_bytes(inputs):
@@ -329,7 +413,7 @@ def run_reference(args, w):
     done_units, secs = 0.0, 0.0
     desc = ""
     for _ in range(args.steps):
-        u, s, desc = cpu_oracle_sample(w, inputs, budget)
+        u, s, desc, _ = cpu_oracle_sample(w, inputs, budget)
         done_units += u
         secs += s
     value = rate(done_units, secs, unit)
@@ -413,11 +497,51 @@ def kernel_source(w):
     return KERNEL_SOURCES[w.kind]
 
 
-def kernel_source_sha(w):
+def _local_includes(path):
+    """Files named by the #include "..." lines of a source (csrc/ or include/)."""
+    import re
+    dirs = [os.path.dirname(path), os.path.join(ROOT, "include")]
+    out = []
+    with open(path, encoding="utf-8") as f:
+        for name in re.findall(r'^\s*#\s*include\s+"([^"]+)"', f.read(), flags=re.M):
+            for d in dirs:
+                cand = os.path.join(d, name)
+                if os.path.exists(cand):
+                    out.append(os.path.normpath(cand))
+                    break
+    return out
+
+
+def kernel_source_files(w):
+    """The dominant kernel's .cu file and every local header it includes,
+    directly or through other headers, in a fixed order."""
+    root = os.path.join(ROOT, "online_softmax_tiled_gb300", "csrc", kernel_source(w))
+    seen, todo = [], [root]
+    while todo:
+        p = todo.pop(0)
+        if p in seen:
+            continue
+        seen.append(p)
+        todo.extend(_local_includes(p))
+    return [seen[0]] + sorted(seen[1:])
+
+
+def hash_sources(paths):
+    """Short hash over the names (relative to the repository) and contents of
+    the given files, in order."""
     import hashlib
-    path = os.path.join(ROOT, "online_softmax_tiled_gb300", "csrc", kernel_source(w))
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in paths:
+        h.update(os.path.relpath(path, ROOT).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_source_sha(w):
+    """Hash of the dominant kernel's source and of the headers it includes: a
+    change to either makes committed counters stale."""
+    return hash_sources(kernel_source_files(w))
 
 
 def profiled_traffic(w):
@@ -434,54 +558,28 @@ def profiled_traffic(w):
     return entry.get("dram_bytes_per_launch")
 
 
-def run_gpu(args, w):
+def make_step(ost, w, x, dev, stream):
+    """One step of the workload's hot path on device-resident inputs ``x``:
+    returns (step callable, kernel launches per step, {output name: tensor})."""
     import torch
-    import torch.distributed as dist
-
-    import online_softmax_tiled_gb300 as ost
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    if rank == 0:
-        import __graft_entry__
-        __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
-    ost.lib()
-    stream = torch.cuda.current_stream(dev)
-
-    host = make_workload_inputs(w)
-    x = {k: t.to(dev) for k, t in host.items()}
-    units, unit, bound = algorithmic_units(w, host)
-    in_bytes = sum(t.numel() * t.element_size() for t in host.values())
-    flush = in_bytes < L2_BYTES
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
-
-    # --- one step of the hot path, device-resident inputs
-    if w.kind == "fwd" and w.masked:
+    if w.kind == "fwd":
         o = torch.empty_like(x["q"])
         lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
-        amask = ost.make_mask(w.window_left, w.window_right, w.n_global, x.get("row_kv_start"),
-                              x.get("row_kv_end"))
-        step = lambda: ost.attn_fwd_masked(x["q"], x["k"], x["v"], o, lse, w.scale, amask, stream)
-        launches_per_step = 1
-        outs = (o, lse)
-    elif w.kind == "fwd":
-        o = torch.empty_like(x["q"])
-        lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
-        step = lambda: ost.attn_fwd(x["q"], x["k"], x["v"], o, lse, w.scale, w.causal, stream)
-        launches_per_step = 1
-        outs = (o, lse)
-    elif w.kind == "bwd":
+        if w.masked:
+            amask = ost.make_mask(w.window_left, w.window_right, w.n_global,
+                                  x.get("row_kv_start"), x.get("row_kv_end"))
+            step = lambda: ost.attn_fwd_masked(x["q"], x["k"], x["v"], o, lse, w.scale, amask,
+                                               stream)
+        else:
+            step = lambda: ost.attn_fwd(x["q"], x["k"], x["v"], o, lse, w.scale, w.causal,
+                                        stream)
+        return step, 1, {"o": o, "lse": lse}
+    if w.kind == "bwd":
         amask = (ost.make_mask(w.window_left, w.window_right, w.n_global) if w.masked
                  else None)
         o, lse = ost.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, mask=amask)
-        ws = torch.empty(ost.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d),
+        ws = torch.empty(ost.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d,
+                                                     w.torch_dtype),
                          dtype=torch.uint8, device=dev)
         dq, dk, dv = (torch.empty_like(x[n]) for n in ("q", "k", "v"))
         if w.masked:
@@ -490,36 +588,45 @@ def run_gpu(args, w):
         else:
             step = lambda: ost.attn_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, dq, dk, dv,
                                         w.scale, w.causal, ws, stream)
-        launches_per_step = 3
-        outs = (dq, dk, dv)
-    elif w.kind == "decode_sparse":
-        ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq * w.Nq, w.d, w.num_splits),
-                         dtype=torch.uint8, device=dev)
-        o = torch.empty_like(x["q"])
-        lse = torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=dev)
+        return step, 3, {"dq": dq, "dk": dk, "dv": dv}
+    rows = w.Hq * w.Nq if w.kind == "decode_sparse" else w.Hq
+    ws = torch.empty(ost.attn_decode_workspace_size(w.B, rows, w.d, w.num_splits),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(x["q"].shape[:-1], dtype=torch.float32, device=dev)
+    if w.kind == "decode_sparse":
         step = lambda: ost.attn_decode_sparse(x["q"], x["k"], x["v"], x["indices"], x["counts"],
                                               o, lse, w.scale, w.num_splits, ws, stream)
-        launches_per_step = 2
-        outs = (o, lse)
     elif w.kind == "decode_paged":
-        ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq, w.d, w.num_splits),
-                         dtype=torch.uint8, device=dev)
-        o = torch.empty_like(x["q"])
-        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
         step = lambda: ost.attn_decode_paged(x["q"], x["k_pages"], x["v_pages"],
                                              x["block_table"], x["seq_lens"], o, lse, w.scale,
                                              w.num_splits, ws, stream)
-        launches_per_step = 2
-        outs = (o, lse)
     else:
-        ws = torch.empty(ost.attn_decode_workspace_size(w.B, w.Hq, w.d, w.num_splits),
-                         dtype=torch.uint8, device=dev)
-        o = torch.empty_like(x["q"])
-        lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
         step = lambda: ost.attn_decode_splitkv(x["q"], x["k"], x["v"], o, lse, w.scale,
                                                w.num_splits, ws, stream)
-        launches_per_step = 2
-        outs = (o, lse)
+    return step, 2, {"o": o, "lse": lse}
+
+
+class ParityError(RuntimeError):
+    pass
+
+
+def measure(args, w, ost, dev, world, rank, stream):
+    """Warm up, check one step against the oracle (rank 0, the CPU-baseline
+    leg), time ``args.steps`` steps and the end-to-end path; returns the
+    workload's entry on rank 0 (None elsewhere)."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    host = make_workload_inputs(w)
+    x = {k: t.to(dev) for k, t in host.items()}
+    units, unit, bound = algorithmic_units(w, host)
+    in_bytes = sum(t.numel() * t.element_size() for t in host.values())
+    flush = in_bytes < L2_BYTES
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    step, launches_per_step, out_map = make_step(ost, w, x, dev, stream)
+    outs = tuple(out_map.values())
 
     def barrier():
         if world > 1:
@@ -530,25 +637,39 @@ def run_gpu(args, w):
         if flush:
             flush_buf.fill_(1)
         step()
-    assert ost.attn_sync_status(stream) == ost.ATTN_OK
+    if ost.attn_sync_status(stream) != ost.ATTN_OK:
+        raise RuntimeError(f"{w.name}: device error after the warm-up steps")
 
     if args.profile:
         # Short run for ncu: warm-up plus `steps` launches, nothing else.
         for _ in range(args.steps):
             step()
         torch.cuda.synchronize(dev)
-        assert ost.attn_sync_status(stream) == ost.ATTN_OK
-        if world > 1:
-            dist.destroy_process_group()
-        return 0
+        if ost.attn_sync_status(stream) != ost.ATTN_OK:
+            raise RuntimeError(f"{w.name}: device error in the profiled steps")
+        return None
+
+    # --- the CPU-baseline leg: the oracle on a bounded sample of this step,
+    # compared with the GPU's outputs of the same units before any timing
+    cpu = None
+    if rank == 0:
+        from workloads import to_f64
+        gpu_host = {n: to_f64(t) for n, t in out_map.items()}
+        cpu_units, cpu_s, cpu_desc, tally = cpu_oracle_sample(w, host, args.cpu_budget,
+                                                              gpu_outs=gpu_host)
+        parity = tally.report()
+        bad = parity_failures(w, parity)
+        if bad:
+            raise ParityError(f"{w.name}: GPU result differs from the oracle: " + "; ".join(bad))
+        cpu = (cpu_units, cpu_s, cpu_desc, parity)
+        del gpu_host
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    if sampler:
-        # bring clocks up before the timed region
-        t_end = time.time() + 0.5
-        while time.time() < t_end:
-            step()
-        torch.cuda.synchronize(dev)
+    # bring clocks up before the timed region
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        step()
+    torch.cuda.synchronize(dev)
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -565,9 +686,10 @@ def run_gpu(args, w):
     if sampler:
         sampler.mark_end()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    total_ms = max_over_ranks(total_ms, dev)
-    assert ost.attn_sync_status(stream) == ost.ATTN_OK
+    total_ms = max_over_ranks(sum(step_ms), dev)
+    if ost.attn_sync_status(stream) != ost.ATTN_OK:
+        raise RuntimeError(f"{w.name}: device error in the timed steps")
+    clocks = sampler.stop() if sampler else None
 
     # --- end to end through the public API: pinned host inputs in, results out
     host_pinned = {k: t.pin_memory() for k, t in host.items()}
@@ -593,27 +715,26 @@ def run_gpu(args, w):
         e2e_step()
     e_e.record(stream)
     barrier()
-    e2e_ms = e_s.elapsed_time(e_e) / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e) / e2e_steps, dev)
+    if ost.attn_sync_status(stream) != ost.ATTN_OK:
+        raise RuntimeError(f"{w.name}: device error in the end-to-end steps")
 
-    clocks = sampler.stop() if sampler else None
-
+    entry = None
     if rank == 0:
         ms_per_step = total_ms / args.steps
-        value = whole_job_rate(units * args.steps, world, total_ms / 1e3, unit)
-        hbm, tf_burst, tf_sust, src = load_peaks()
+        hbm, tf_burst, _tf_sust, src = load_peaks()
         peak = hbm if bound == "hbm" else tf_burst
         peak_source = f"{src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops burst'})"
         if w.dtype == "f32":
             # float32 FFMA path: 152 SMs x 128 FMA lanes x 2 flops x 2.07 GHz max clock
             bound, peak, peak_source = "alu", FP32_FFMA_PEAK_TFLOPS, "derived (FFMA lanes x clock)"
         achieved = rate(units, ms_per_step / 1e3, unit)
-        cpu_units, cpu_s, cpu_desc = cpu_oracle_sample(w, host, args.cpu_budget)
-        line = {
-            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, flush),
+        cpu_units, cpu_s, cpu_desc, parity = cpu
+        entry = {
+            "value": whole_job_rate(units * args.steps, world, total_ms / 1e3, unit),
+            "unit": unit, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "dtype": w.dtype,
+            "config": workload_config(w, flush),
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                          "unit": unit, "frac": achieved / peak,
                          "peak_source": peak_source,
@@ -622,15 +743,68 @@ def run_gpu(args, w):
             "cpu_baseline": {"value": rate(cpu_units, cpu_s, unit), "unit": unit,
                              "cores": host_cores(), "kind": "oracle",
                              "sample": f"{cpu_desc} of one step, float64 NumPy, {cpu_s:.1f} s"},
+            "parity": {"checked": f"{cpu_desc} of one warm-up step against the float64 oracle "
+                                  "before timing",
+                       "outputs": parity},
             "e2e": {"value": whole_job_rate(units, world, e2e_ms / 1e3, unit), "unit": unit,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
+    del x, outs, out_map, step, host_pinned, out_host, flush_buf
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_gpu(args, w, extras):
+    import torch
+    import torch.distributed as dist
+
+    import online_softmax_tiled_gb300 as ost
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    ost.lib()
+    stream = torch.cuda.current_stream(dev)
+
+    rc = 0
+    try:
+        main_entry = measure(args, w, ost, dev, world, rank, stream)
+        extra_entries = {}
+        for e in extras:
+            extra_entries[e.name] = measure(args, e, ost, dev, world, rank, stream)
+    except ParityError as err:
+        print(str(err), file=sys.stderr)
+        rc = 1
+    if rc == 0 and rank == 0 and not args.profile:
+        line = {"metric": METRIC, "value": main_entry["value"], "unit": main_entry["unit"],
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": main_entry["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic"}
+        for key in ("config", "roofline", "cpu_baseline", "parity", "e2e", "gpu_launches",
+                    "clocks"):
+            line[key] = main_entry[key]
+        if extra_entries:
+            line["workloads"] = extra_entries
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
-    return 0
+    return rc
+
+
+DEFAULT_WORKLOAD = "fwd_causal_n8192_d128"
+DEFAULT_EXTRA = "bwd_causal_n4096_d128,decode_gqa_l4096,fwd_mha_n2048_d64"
 
 
 def main():
@@ -640,9 +814,13 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="fwd_mha_n2048_d64", choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of CPU oracle work for the cpu_baseline figure")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--extra", default=None,
+                    help="comma-separated workloads timed after the top-level one and "
+                         "reported under 'workloads' ('none': no others); default: "
+                         f"{DEFAULT_EXTRA} when --workload is the default, else none")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of CPU oracle work for each cpu_baseline figure")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up and timed launches, no JSON line (for ncu captures)")
     args = ap.parse_args()
@@ -651,7 +829,14 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
-    return run_gpu(args, w)
+    extra = args.extra
+    if extra is None:
+        extra = DEFAULT_EXTRA if args.workload == DEFAULT_WORKLOAD else "none"
+    names = [n for n in extra.split(",") if n and n != "none" and n != w.name]
+    for n in names:
+        if n not in WORKLOADS:
+            ap.error(f"unknown workload in --extra: {n}")
+    return run_gpu(args, w, [WORKLOADS[n] for n in names])
 
 
 if __name__ == "__main__":

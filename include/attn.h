@@ -36,6 +36,13 @@
  * Device-side waits. Every wait inside a kernel is bounded; a wait that runs
  *   out sets a library error word and the kernel returns. attn_sync_status()
  *   reports that as ATTN_ERR_DEVICE_TIMEOUT.
+ * Error word scope. The device error word is one per device for the whole
+ *   process: every call and every stream on that device sets the same word,
+ *   and attn_sync_status() reports and clears it for whichever caller polls
+ *   first. With several streams (or threads) on one device, a timeout or a
+ *   bad index raised by work on one stream can therefore be reported to, and
+ *   cleared by, a caller that polls another; callers that need to attribute
+ *   a device error to a call must poll with no other work in flight.
  */
 #ifndef ONLINE_SOFTMAX_TILED_GB300_ATTN_H
 #define ONLINE_SOFTMAX_TILED_GB300_ATTN_H
@@ -131,10 +138,22 @@ ATTN_API attn_status attn_fwd_masked(const void* q, const void* k, const void* v
                                      void* stream);
 
 /*
- * Bytes of device scratch attn_bwd needs: the row term D [B,Hq,Nq] float32
- * and a float32 dQ accumulator [B,Hq,Nq,d], each 256-byte aligned.
+ * Bytes of device scratch attn_bwd needs for any dtype: the row term D
+ * [B,Hq,Nq] float32 and a float32 dQ accumulator [B,Hq,Nq,d], each 256-byte
+ * aligned. This is the largest need; attn_bwd_workspace_size_dt gives the
+ * exact need of one dtype.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
+
+/*
+ * Bytes of device scratch attn_bwd (and attn_bwd_masked) use for dtype `dt`:
+ * with dt = ATTN_BF16 and d = 128 only the row term D [B,Hq,Nq] float32
+ * (256-byte aligned), because the dQ pass writes dQ directly; otherwise the
+ * row term followed by the float32 dQ accumulator, as
+ * attn_bwd_workspace_size. 0 for invalid arguments.
+ */
+ATTN_API size_t attn_bwd_workspace_size_dt(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                           attn_dtype dt);
 
 /*
  * Backward pass by recomputation.
@@ -157,8 +176,9 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, 
  *
  * Inputs: q, k, v, o (forward output), dO, lse (forward LSE), all in `dt`
  * except lse (float32). Outputs dq, dk, dv in `dt`, overwritten.
- * workspace: device scratch of at least attn_bwd_workspace_size() bytes,
- * 256-byte aligned; its contents on entry do not matter.
+ * workspace: device scratch of at least attn_bwd_workspace_size_dt(..., dt)
+ * bytes (attn_bwd_workspace_size() is always enough), 256-byte aligned; its
+ * contents on entry do not matter.
  * dt = ATTN_BF16 with d in {64, 128}; ATTN_F32 with d in {64, 128}.
  */
 ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -313,7 +333,10 @@ ATTN_API attn_status attn_merge_partials(const float* o_part, const float* m_par
  *
  * Set-up: the first call on a device looks up that device's address of the
  * array (cudaGetSymbolAddress, with the device current) and caches it; make
- * that first call before any stream capture on the device.
+ * that first call before any stream capture on the device. The cached
+ * address belongs to the device's current context: after cudaDeviceReset()
+ * on that device it is stale, and this entry point must not be called again
+ * in that process.
  *
  * Sharing: all calls on a device use the same array. Nothing in it needs to
  * start at zero (each call writes every partial it reads), but calls whose
@@ -326,6 +349,21 @@ ATTN_API attn_status attn_decode_splitkv_noalloc(const void* q, const void* k_ca
                                                  const void* v_cache, void* o, float* lse, int B,
                                                  int Hq, int Hkv, int L, int d, float scale,
                                                  int num_splits, void* stream);
+
+/*
+ * Self-test of the bounded device wait (no counterpart on the pages).
+ *
+ * Launches one warp on `stream` that waits, with the same bounded wait the
+ * kernels use, on a barrier nothing ever arrives on, for `limit_us`
+ * microseconds (1 .. 1,000,000); then it records a timeout in the device
+ * error word and exits. Nothing asynchronous is in flight while it waits, so
+ * the context stays usable: a following attn_sync_status() returns
+ * ATTN_ERR_DEVICE_TIMEOUT (and clears the word), and later calls run
+ * normally. It shows that a wait that runs out reaches the caller as a
+ * status instead of a hang. Returns ATTN_ERR_INVALID_ARG for a limit out of
+ * range, ATTN_ERR_CUDA if the launch fails, else ATTN_OK.
+ */
+ATTN_API attn_status attn_selftest_bounded_wait(unsigned int limit_us, void* stream);
 
 /* Static, human-readable name of a status code. */
 ATTN_API const char* attn_status_string(attn_status s);

@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_masked,
     attn_bwd_workspace_size,
+    attn_selftest_bounded_wait,
     attn_decode_paged,
     attn_decode_sparse,
     attn_decode_splitkv,

@@ -52,6 +52,8 @@ _SIGNATURES = {
                         [ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                          ctypes.c_size_t, ctypes.c_void_p]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 6),
+    "attn_bwd_workspace_size_dt": (ctypes.c_size_t, [ctypes.c_int] * 7),
+    "attn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint, ctypes.c_void_p]),
     "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 6 +
                  [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                   ctypes.c_void_p]),
@@ -162,8 +164,15 @@ def attn_fwd_masked(q, k, v, o, lse, scale: float, mask, stream=None):
     _check(st, "attn_fwd_masked")
 
 
-def attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d) -> int:
-    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d))
+def attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d, dtype=None) -> int:
+    """Workspace bytes of attn_bwd: for ``dtype`` (torch.float32 or
+    torch.bfloat16) the exact need, else the largest over dtypes."""
+    if dtype is None:
+        return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, Nq, Nk, d))
+    dt = ATTN_F32 if dtype == torch.float32 else ATTN_BF16 if dtype == torch.bfloat16 else None
+    if dt is None:
+        raise TypeError(f"unsupported dtype {dtype}: float32 or bfloat16")
+    return int(lib().attn_bwd_workspace_size_dt(B, Hq, Hkv, Nq, Nk, d, dt))
 
 
 def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, scale: float, causal: bool, workspace,
@@ -274,6 +283,13 @@ def attn_sync_status(stream=None) -> int:
     return int(lib().attn_sync_status(_stream(stream)))
 
 
+def attn_selftest_bounded_wait(limit_us: int, stream=None):
+    """Launch the bounded-wait self-test (a wait that runs out after
+    ``limit_us``); the next attn_sync_status reports the timeout."""
+    _check(lib().attn_selftest_bounded_wait(int(limit_us), _stream(stream)),
+           "attn_selftest_bounded_wait")
+
+
 # ------------------------------------------- allocating conveniences (torch)
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, with_lse: bool = True,
@@ -297,7 +313,7 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     forward's mask, replaces ``causal`` when given)."""
     B, Hq, Nq, d = q.shape
     scale = d ** -0.5 if scale is None else scale
-    ws = torch.empty(attn_bwd_workspace_size(B, Hq, k.shape[1], Nq, k.shape[2], d),
+    ws = torch.empty(attn_bwd_workspace_size(B, Hq, k.shape[1], Nq, k.shape[2], d, q.dtype),
                      dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if mask is not None:

@@ -41,6 +41,15 @@ BwdLayout bwd_layout(int B, int Hq, int Nq, int d) {
   return l;
 }
 
+// bf16 at d = 128 runs the dQ query-tile pass, which writes dQ directly: only
+// the row term is needed. Every other path also adds dQ into the float32
+// accumulator that follows it.
+inline bool bwd_split_dq(int d, attn_dtype dt) { return dt == ATTN_BF16 && d == 128; }
+
+size_t bwd_workspace_need(const BwdLayout& l, int d, attn_dtype dt) {
+  return bwd_split_dq(d, dt) ? l.dq_acc : l.total;
+}
+
 struct DecodeLayout {
   size_t o_part, m_part, l_part, total;
 };
@@ -144,6 +153,15 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d) {
   return bwd_layout(B, Hq, Nq, d).total;
 }
 
+size_t attn_bwd_workspace_size_dt(int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                  attn_dtype dt) {
+  (void)Hkv;
+  (void)Nk;
+  if (B <= 0 || Hq <= 0 || Nq <= 0 || d <= 0) return 0;
+  if (dt != ATTN_F32 && dt != ATTN_BF16) return 0;
+  return bwd_workspace_need(bwd_layout(B, Hq, Nq, d), d, dt);
+}
+
 namespace {
 
 attn_status bwd_common(const void* q, const void* k, const void* v, const void* o,
@@ -156,7 +174,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   for (const void* p : ptrs)
     if (!aligned16(p)) return ATTN_ERR_MISALIGNED;
   const BwdLayout lay = bwd_layout(B, Hq, Nq, d);
-  if (!workspace || ws_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < bwd_workspace_need(lay, d, dt)) return ATTN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
   const bool plain = ms.window_left < 0 && ms.window_right <= 0 && ms.n_global == 0 &&
                      ms.row_kv_start == nullptr;
@@ -173,7 +191,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   // bf16, d = 128: a key-tile pass (dK, dV) and a query-tile pass (dQ, written
   // in bf16 directly; the float32 accumulator is not used). Otherwise one
   // pass adds dQ into the float32 accumulator, converted at the end.
-  const bool split_dq = dt == ATTN_BF16 && d == 128;
+  const bool split_dq = bwd_split_dq(d, dt);
   a.zero_dq_acc = !split_dq;
   cudaError_t e = launch_bwd_preprocess(a);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;

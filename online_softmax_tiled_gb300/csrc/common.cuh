@@ -185,7 +185,8 @@ ATTN_DEVINL bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // is first read after 256 unsuccessful probes: reading %globaltimer costs
 // about 100 cycles, which a wait that succeeds at once must not pay (measured
 // on GB300: 119 vs 17 cycles per completed-phase wait).
-ATTN_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+ATTN_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                   uint64_t limit_ns = kWaitLimitNs) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -194,7 +195,7 @@ ATTN_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int*
       const uint64_t now = global_timer_ns();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         return false;
       }
     }

@@ -657,3 +657,35 @@ extern "C" ATTN_API attn_status attn_decode_splitkv_noalloc(const void* q, const
 }
 
 }  // namespace attn
+
+// ----------------------------------------------------------------------------
+// attn_selftest_bounded_wait: one warp waits, through the bounded wait that
+// every kernel of the library uses, on an mbarrier that nothing will ever
+// arrive on. When the limit runs out it records the timeout in the error word
+// and returns, as a kernel does when a real wait runs out. Nothing
+// asynchronous (bulk copy, tensor-core op) is in flight at any time.
+// ----------------------------------------------------------------------------
+namespace attn {
+namespace {
+
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0, nullptr, limit_ns))
+    attn_flag_error(kErrTimeout);
+}
+
+}  // namespace
+
+extern "C" ATTN_API attn_status attn_selftest_bounded_wait(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return ATTN_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      uint64_t(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn

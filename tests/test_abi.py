@@ -68,6 +68,15 @@ def test_workspace_sizes(lib):
     assert lib.attn_decode_workspace_size(B, Hq, d, S) == _a256(n * d * 4) + 2 * _a256(n * 4)
     assert lib.attn_bwd_workspace_size(0, 1, 1, 1, 1, 64) == 0
     assert lib.attn_decode_workspace_size(1, 1, 64, 0) == 0
+    # per dtype: bf16 at d = 128 writes dQ directly and needs only the row term
+    B, H, N = 2, 16, 4096
+    rows = B * H * N
+    assert lib.attn_bwd_workspace_size_dt(B, H, H, N, N, 128, 1) == _a256(rows * 4)
+    for d, dt in ((64, 1), (128, 0), (64, 0)):
+        assert lib.attn_bwd_workspace_size_dt(B, H, H, N, N, d, dt) == \
+            lib.attn_bwd_workspace_size(B, H, H, N, N, d)
+    assert lib.attn_bwd_workspace_size_dt(B, H, H, N, N, 128, 7) == 0
+    assert lib.attn_bwd_workspace_size_dt(0, H, H, N, N, 128, 1) == 0
 
 
 P = 1 << 20  # a 16-byte aligned stand-in address; never dereferenced on these paths
@@ -112,6 +121,11 @@ def test_bwd_rejects_before_launch(lib):
     bad = list(args)
     bad[14] = 80   # d
     assert lib.attn_bwd(*bad, P, need, None) == UNSUPPORTED
+    # bf16 at d = 128 checks the workspace against its own (smaller) need
+    args128 = [P] * 9 + [1, 2, 2, 16, 16, 128, 0.125, 1, 1]
+    need128 = lib.attn_bwd_workspace_size_dt(1, 2, 2, 16, 16, 128, 1)
+    assert need128 < lib.attn_bwd_workspace_size(1, 2, 2, 16, 16, 128)
+    assert lib.attn_bwd(*args128, P, need128 - 1, None) == WORKSPACE
 
 
 def test_decode_rejects_before_launch(lib):

@@ -1,7 +1,9 @@
 """GPU split-KV decode and merge vs the float64 oracle.
 
-Tolerance: bf16 O max|err| <= 2e-2, LSE <= 1e-3 (benchmark description);
-the merge kernel on float32 partials: 1e-5 relative to max|O|.
+Tolerance: bf16 O max|err| <= 2e-2, LSE <= 1e-3 (benchmark description),
+and O also max|err| <= 1e-2 * max|O| (with N(0,1) inputs |O| is a few
+hundredths, so the absolute bound alone would be weak); the merge kernel on
+float32 partials: 1e-5 relative to max|O|.
 """
 
 import numpy as np
@@ -23,9 +25,12 @@ def _check(ost, w, scale=None):
     o_ref, lse_ref = oracle.decode_splitkv(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), scale,
                                            w.num_splits)
     err_o = np.max(np.abs(to_f64(o) - o_ref))
-    assert err_o <= 2e-2, err_o
+    mx = np.max(np.abs(o_ref))
+    msg = (f"max|err| {err_o:.3e}", f"max|ref| {mx:.3e}", f"rel {err_o / mx:.3e}")
+    assert err_o <= 2e-2, msg
+    assert err_o <= 1e-2 * mx, msg
     assert np.max(np.abs(to_f64(lse) - lse_ref)) <= 1e-3
-    return err_o, np.max(np.abs(o_ref))
+    return err_o, mx
 
 
 def test_gqa_decode_workload_full(ost):

@@ -30,16 +30,31 @@ def _run(ost, w, scale=None, with_lse=True):
     return x, o, lse, scale
 
 
+# bf16 outputs are also held to a bound relative to the largest |O|: with
+# N(0,1) inputs |O| is only a few hundredths, so the absolute 2e-2 alone
+# would let a large relative error through. The expected relative error is
+# a few 1e-3 (bf16 rounding of O and of P before P·V).
+REL_O = 1e-2
+
+
+def _assert_o(got, ref, dtype, where=""):
+    err = float(np.max(np.abs(got - ref)))
+    mx = float(np.max(np.abs(ref)))
+    tol = _tol(dtype)[0]
+    msg = (where, f"max|err| {err:.3e}", f"max|ref| {mx:.3e}", f"rel {err / mx:.3e}")
+    assert err <= tol, msg
+    if dtype == "bf16":
+        assert err <= REL_O * mx, msg
+
+
 def _check_full(ost, w, scale=None):
     x, o, lse, scale = _run(ost, w, scale)
     o_ref, lse_ref = oracle.attention_fwd(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]), scale,
                                           w.causal)
     tol_o, tol_l = _tol(w.dtype)
-    err_o = np.max(np.abs(to_f64(o) - o_ref))
+    _assert_o(to_f64(o), o_ref, w.dtype, w.name)
     err_l = np.max(np.abs(to_f64(lse) - lse_ref))
-    assert err_o <= tol_o, (err_o, np.max(np.abs(o_ref)))
     assert err_l <= tol_l, err_l
-    return err_o, err_l
 
 
 def test_f32_single_head_workload(ost):
@@ -112,5 +127,5 @@ def test_causal_long_workload_sampled(ost):
     for b, h in [(0, 0), (1, 31), (0, 17), (1, 5)]:
         rows = np.unique(np.concatenate([fixed, rng.integers(0, w.Nq, 20)]))
         o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, scale, True, b, h, rows)
-        assert np.max(np.abs(o[b, h, rows] - o_ref)) <= 2e-2
+        _assert_o(o[b, h, rows], o_ref, "bf16", (b, h))
         assert np.max(np.abs(lse[b, h, rows] - lse_ref)) <= 1e-3

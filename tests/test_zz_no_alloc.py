@@ -5,9 +5,10 @@ memory at decode time (memory partitioned up front, or a host program that
 owns every allocation): its split partials live in a fixed array inside the
 library instead of a caller workspace. Here it is called through the C ABI
 twice in a row, on different inputs, and each result is compared with the
-workspace entry point's result for the same inputs, within the decode
-tolerance used by the other tests (O 2e-2, LSE 1e-3). This file is collected
-last so that a failure here cannot hide any other test.
+workspace entry point's result for the same inputs and with the float64
+oracle, within the decode tolerance used by the other tests (O 2e-2, LSE
+1e-3). This file is collected last so that a failure here cannot hide any
+other test.
 """
 
 import ctypes
@@ -16,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from workloads import Workload, make_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -48,6 +50,10 @@ def test_noalloc_decode_matches_workspace_decode_twice(ost):
         assert ost.attn_sync_status() == 0
         assert np.max(np.abs(to_f64(o) - to_f64(o_ref))) <= 2e-2
         assert np.max(np.abs(to_f64(lse) - to_f64(lse_ref))) <= 1e-3
+        o64, lse64 = oracle.decode_splitkv(to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"]),
+                                           w.scale, w.num_splits)
+        assert np.max(np.abs(to_f64(o) - o64)) <= 2e-2
+        assert np.max(np.abs(to_f64(lse) - lse64)) <= 1e-3
 
 
 def test_noalloc_decode_rejects_oversized_partials(ost):
