@@ -28,22 +28,25 @@ attn_status check_attention_shapes(int B, int Hq, int Hkv, int Nq, int Nk, int d
   return ATTN_OK;
 }
 
+// Row term D, then 256 bytes for the persistent dQ pass's work counter, then
+// the float32 dQ accumulator.
 struct BwdLayout {
-  size_t row_term, dq_acc, total;
+  size_t row_term, sched, dq_acc, total;
 };
 
 BwdLayout bwd_layout(int B, int Hq, int Nq, int d) {
   BwdLayout l;
   const size_t rows = size_t(B) * Hq * Nq;
   l.row_term = 0;
-  l.dq_acc = align256(rows * sizeof(float));
+  l.sched = align256(rows * sizeof(float));
+  l.dq_acc = l.sched + 256;
   l.total = l.dq_acc + align256(rows * d * sizeof(float));
   return l;
 }
 
 // bf16 at d = 128 runs the dQ query-tile pass, which writes dQ directly: only
-// the row term is needed. Every other path also adds dQ into the float32
-// accumulator that follows it.
+// the row term and the counter are needed. Every other path also adds dQ
+// into the float32 accumulator that follows them.
 inline bool bwd_split_dq(int d, attn_dtype dt) { return dt == ATTN_BF16 && d == 128; }
 
 size_t bwd_workspace_need(const BwdLayout& l, int d, attn_dtype dt) {
@@ -188,6 +191,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
             reinterpret_cast<float*>(ws + lay.row_term), reinterpret_cast<float*>(ws + lay.dq_acc),
             static_cast<cudaStream_t>(stream), true};
   a.mask = ms;
+  if (bwd_persistent(d, dt, ms)) a.sched = reinterpret_cast<int*>(ws + lay.sched);
   // bf16, d = 128: a key-tile pass (dK, dV) and a query-tile pass (dQ, written
   // in bf16 directly; the float32 accumulator is not used). Otherwise one
   // pass adds dQ into the float32 accumulator, converted at the end.

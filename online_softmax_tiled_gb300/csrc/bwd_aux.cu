@@ -6,7 +6,8 @@
 // rowsum(P ∘ dP) = Σ_j P_ij Σ_c dO_ic V_jc = Σ_c dO_ic O_ic, so the row term
 // D_i = rowsum(dO ∘ O) is computed here from O and dO in one streaming pass,
 // before the main backward kernels run. When a pass adds dQ into the float32
-// accumulator (d = 64, float32 inputs), the same pass zeroes it first.
+// accumulator (d = 64, float32 inputs), the same pass zeroes it first; when
+// the dQ pass is persistent, it zeroes its work counter.
 //
 // dQ conversion. After the main kernel, dQ = dtype(dQ_acc) (round to nearest
 // even for bf16); the bf16 d = 128 path writes dQ directly and skips it.
@@ -23,10 +24,13 @@ namespace {
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
 bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dO,
-                      float* __restrict__ row_term, float* __restrict__ dq_acc, long rows) {
+                      float* __restrict__ row_term, float* __restrict__ dq_acc,
+                      int* __restrict__ sched, long rows) {
   // the key-tile pass (d = 128) may launch while this grid's last blocks run;
-  // it waits for this grid before reading the row term
+  // it waits for this grid before reading the row term, and lets the dQ
+  // pass (which reads the row term and the work counter) start only after
   pdl_launch_dependents();
+  if (sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   const int lane = threadIdx.x & 31;
   if constexpr (sizeof(T) == 2) {
     constexpr int kLanesPerRow = D / 8;
@@ -93,10 +97,10 @@ cudaError_t launch_pre_t(const BwdArgs& a) {
   float* acc = a.zero_dq_acc ? a.dq_acc : nullptr;
   if (a.d == 64)
     bwd_preprocess_kernel<T, 64><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const T*>(a.o), static_cast<const T*>(a.dO), a.row_term, acc, rows);
+        static_cast<const T*>(a.o), static_cast<const T*>(a.dO), a.row_term, acc, a.sched, rows);
   else
     bwd_preprocess_kernel<T, 128><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const T*>(a.o), static_cast<const T*>(a.dO), a.row_term, acc, rows);
+        static_cast<const T*>(a.o), static_cast<const T*>(a.dO), a.row_term, acc, a.sched, rows);
   return cudaGetLastError();
 }
 

@@ -176,6 +176,79 @@ ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* do
   tc::mma_commit_warp(done);
 }
 
+// One thread's share of a step's softmax backward, keys on the TMEM lanes:
+// its key row (lane r, key index `key`) and its warpgroup's CW query
+// columns from cbase, in (Sᵀ, dPᵀ) buffer b and Q stage st. Pᵀ =
+// exp2(Sᵀ·scale·log2e - LSE·log2e) and dSᵀ = Pᵀ ∘ (dPᵀ - D) (d = 128: the
+// -LSE/scale and -D terms are already in the scores; d = 64: read per
+// column from the stage's vectors), as bf16 pairs written back over the
+// columns just read (the A operands of dV and dK); d = 64 also writes a dSᵀ
+// copy to shared memory for dQ. masked_row: some column may be hidden, then
+// (no general mask) columns before qmin and every column of a key past Nk
+// get P = 0, or (general mask) the columns whose row interval in keys_st
+// does not contain the key.
+template <int D, bool kGeneral>
+ATTN_DEVINL void bwd_pds_step(uint8_t* smem, uint32_t tmem, uint32_t lane_base, int b, int st,
+                              int r, int key, bool key_in, int cbase, int qmin, bool masked_row,
+                              float c, const int4* keys_st) {
+  using C = BwdCfg<D>;
+  constexpr int BQ = C::BQ;
+  constexpr int CW = BQ / 2;
+  const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * BQ * 4);
+  uint8_t* dst = smem + C::kOffP;
+  const f2 c2{c, c};
+#pragma unroll
+  for (int chunk = 0; chunk < CW / 32; ++chunk) {
+    uint32_t sr[32], dr[32];
+    const int col0 = cbase + chunk * 32;
+    tc::tmem_ld32(tmem + lane_base + C::col_s(b) + col0, sr);
+    tc::tmem_ld32(tmem + lane_base + C::col_dp(b) + col0, dr);
+    tc::tmem_ld_wait();
+    uint32_t pk[16], dk[16];                  // bf16 pairs of the 32 columns
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {          // 8 columns = one 16-byte chunk of dSᵀ
+#pragma unroll
+      for (int h4 = 0; h4 < 2; ++h4) {
+        const int cb = g8 * 8 + h4 * 4;         // column within the 32
+        // -LSE·log2e and -D per column (d = 64); d = 128 has them in the scores
+        const float4 nl = C::kAugTerms ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                       : *reinterpret_cast<const float4*>(vec + col0 + cb);
+        const float4 nd = C::kAugTerms ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                       : *reinterpret_cast<const float4*>(vec + BQ + col0 + cb);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int e = cb + 2 * u;
+          f2 x = fma2(f2{__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])}, c2,
+                      u == 0 ? f2{nl.x, nl.y} : f2{nl.z, nl.w});
+          f2 p{fast_exp2(x.x), fast_exp2(x.y)};
+          if (masked_row) {
+            const int col = col0 + e;
+            if (kGeneral) {
+              if (!load_row_keys(&keys_st[col]).visible(key)) p.x = 0.f;
+              if (!load_row_keys(&keys_st[col + 1]).visible(key)) p.y = 0.f;
+            } else {
+              if (!key_in || col < qmin) p.x = 0.f;
+              if (!key_in || col + 1 < qmin) p.y = 0.f;
+            }
+          }
+          const f2 dpd = add2(f2{__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])},
+                              u == 0 ? f2{nd.x, nd.y} : f2{nd.z, nd.w});
+          const f2 ds = mul2(p, dpd);
+          pk[e >> 1] = pack_bf16x2(p.x, p.y);
+          dk[e >> 1] = pack_bf16x2(ds.x, ds.y);
+        }
+      }
+      const uint32_t off = sw128_offset(r, col0 + g8 * 8, kBK);
+      if (C::kFusedDq)             // dSᵀ copy for dQ = dS K_j
+        *reinterpret_cast<uint4*>(dst + off) =
+          make_uint4(dk[4 * g8], dk[4 * g8 + 1], dk[4 * g8 + 2], dk[4 * g8 + 3]);
+    }
+    // Pᵀ and dSᵀ pairs over the columns just read (A operands of dV, dK)
+    tc::tmem_st16(tmem + lane_base + C::col_s(b) + C::col_pair(col0), pk);
+    tc::tmem_st16(tmem + lane_base + C::col_dp(b) + C::col_pair(col0), dk);
+  }
+}
+
 // The (head, query tile) steps of one CTA: every query head of the group,
 // and per head the query tiles from the first one that sees key k0 (causal)
 // to the last, or (general masks) the query tiles listed in shared memory.
@@ -258,9 +331,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
               MaskSpec mask, int n_ktiles, int order_grp) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
-  // The dQ pass that follows (d = 128) reads none of this kernel's outputs:
-  // let it start on the SMs this grid's last wave leaves idle.
-  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -389,6 +459,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     // d = 128 launches as a programmatic dependent of the preprocess: the row
     // term D is read only once that grid has completed (a no-op otherwise).
     pdl_wait_primary();
+    // The dQ pass that follows (d = 128) reads none of this kernel's outputs,
+    // only the row term and its work counter, both written by the
+    // preprocess: let it start on the SMs this grid's last wave leaves idle
+    // once every CTA here has seen the preprocess complete.
+    pdl_launch_dependents();
     auto fetch = [&](int s) {
       int hh, qt;
       plan.at(s, hh, qt);
@@ -587,64 +662,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         w = w && mbar_wait_bounded(&bars.ps_free[0], (s - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc::fence_after_sync();
-      const float* vec = reinterpret_cast<const float*>(smem + C::kOffVec + st * 2 * BQ * 4);
-      uint8_t* dst = smem + C::kOffP;
       const bool key_in = key < Nk;
       // first visible query column of this key row (causal), relative to q0;
       // general masks: the step is masked unless every pair is visible
       const int qmin = (!kGeneral && mask.window_right == 0) ? key - shift - q0 : -1;
       const bool masked_row = kGeneral ? stage_clean[st] == 0 : (!key_in || qmin > cbase);
-      const f2 c2{c, c};
-#pragma unroll
-      for (int chunk = 0; chunk < CW / 32; ++chunk) {
-        uint32_t sr[32], dr[32];
-        const int col0 = cbase + chunk * 32;
-        tc::tmem_ld32(tmem + lane_base + C::col_s(b) + col0, sr);
-        tc::tmem_ld32(tmem + lane_base + C::col_dp(b) + col0, dr);
-        tc::tmem_ld_wait();
-        uint32_t pk[16], dk[16];                  // bf16 pairs of the 32 columns
-#pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {          // 8 columns = one 16-byte chunk of dSᵀ
-#pragma unroll
-          for (int h4 = 0; h4 < 2; ++h4) {
-            const int cb = g8 * 8 + h4 * 4;         // column within the 32
-            // -LSE·log2e and -D per column (d = 64); d = 128 has them in the scores
-            const float4 nl = C::kAugTerms ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                           : *reinterpret_cast<const float4*>(vec + col0 + cb);
-            const float4 nd = C::kAugTerms ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                           : *reinterpret_cast<const float4*>(vec + BQ + col0 + cb);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int e = cb + 2 * u;
-              f2 x = fma2(f2{__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])}, c2,
-                          u == 0 ? f2{nl.x, nl.y} : f2{nl.z, nl.w});
-              f2 p{fast_exp2(x.x), fast_exp2(x.y)};
-              if (masked_row) {
-                const int col = col0 + e;
-                if (kGeneral) {
-                  if (!load_row_keys(&stage_keys[st][col]).visible(key)) p.x = 0.f;
-                  if (!load_row_keys(&stage_keys[st][col + 1]).visible(key)) p.y = 0.f;
-                } else {
-                  if (!key_in || col < qmin) p.x = 0.f;
-                  if (!key_in || col + 1 < qmin) p.y = 0.f;
-                }
-              }
-              const f2 dpd = add2(f2{__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])},
-                                  u == 0 ? f2{nd.x, nd.y} : f2{nd.z, nd.w});
-              const f2 ds = mul2(p, dpd);
-              pk[e >> 1] = pack_bf16x2(p.x, p.y);
-              dk[e >> 1] = pack_bf16x2(ds.x, ds.y);
-            }
-          }
-          const uint32_t off = sw128_offset(r, col0 + g8 * 8, kBK);
-          if (C::kFusedDq)             // dSᵀ copy for dQ = dS K_j
-            *reinterpret_cast<uint4*>(dst + off) =
-              make_uint4(dk[4 * g8], dk[4 * g8 + 1], dk[4 * g8 + 2], dk[4 * g8 + 3]);
-        }
-        // Pᵀ and dSᵀ pairs over the columns just read (A operands of dV, dK)
-        tc::tmem_st16(tmem + lane_base + C::col_s(b) + C::col_pair(col0), pk);
-        tc::tmem_st16(tmem + lane_base + C::col_dp(b) + C::col_pair(col0), dk);
-      }
+      bwd_pds_step<D, kGeneral>(smem, tmem, lane_base, b, st, r, key, key_in, cbase, qmin,
+                                masked_row, c, kGeneral ? &stage_keys[st][0] : nullptr);
       tc::tmem_st_wait();
       // generic-proxy writes of the dSᵀ copy -> tensor-core (async proxy) reads
       if (C::kFusedDq) fence_proxy_async_smem();

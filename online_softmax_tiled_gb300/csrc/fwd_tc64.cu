@@ -636,18 +636,6 @@ fwd_tc64_kernel(const __grid_constant__ CUtensorMap map_q,
   }
 }
 
-int sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 template <bool kGeneral>
 cudaError_t launch_t(const FwdArgs& a) {
   CUtensorMap mq, mk, mv, mo;
@@ -664,7 +652,7 @@ cudaError_t launch_t(const FwdArgs& a) {
   if (tiles > 0x7fffffffL) return cudaErrorInvalidValue;
   // one CTA per SM; with per-row key ranges one CTA per tile (the plan is
   // reduced over the tile's rows before the roles start)
-  const int sms = sm_count();
+  const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidValue;
   const bool row_ranges = a.mask.row_kv_start != nullptr;
   const long grid = row_ranges ? tiles : (tiles < sms ? tiles : sms);

@@ -56,6 +56,9 @@ struct BwdArgs {
   cudaStream_t stream;
   bool zero_dq_acc;  // the preprocess zeroes dq_acc (the passes that add into it)
   MaskSpec mask;     // the full mask (causal: window (-1, 0))
+  // Work counter of the persistent dQ pass, zeroed by the preprocess;
+  // nullptr when no persistent pass runs.
+  int* sched = nullptr;
 };
 
 struct DecodeArgs {
@@ -138,6 +141,27 @@ inline int order_group(bool causal, long long bytes_per_head, long long budget =
 
 // Workspace carving (bytes, 256-aligned sections).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Streaming multiprocessors of the current device (cached per device); 0 if
+// it cannot be read.
+inline int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// The bf16 d = 128 backward without a general mask runs its dQ pass as a
+// persistent grid that takes work from a counter in the workspace.
+inline bool bwd_persistent(int d, attn_dtype dt, const MaskSpec& m) {
+  return dt == ATTN_BF16 && d == 128 && m.window_left < 0 && m.window_right <= 0 &&
+         m.n_global == 0 && m.row_kv_start == nullptr;
+}
 
 cudaError_t launch_fwd_simt(const FwdArgs& a);
 cudaError_t launch_fwd_tc(const FwdArgs& a);

@@ -54,6 +54,9 @@ SMALL = [
     (1, 8, 1, 200, 333, 128, "bf16", False),
     (1, 1, 1, 1, 300, 128, "bf16", True),
     (1, 2, 2, 513, 129, 128, "bf16", False),
+    # more 128-row query tiles (176) than SMs: the persistent dQ pass runs
+    # several tiles per CTA, taken from its work counter; GQA 4:1
+    (2, 8, 2, 1400, 1400, 128, "bf16", True),
 ]
 
 
