@@ -139,17 +139,17 @@ ATTN_API attn_status attn_fwd_masked(const void* q, const void* k, const void* v
 
 /*
  * Bytes of device scratch attn_bwd needs for any dtype: the row term D
- * [B,Hq,Nq] float32 and a float32 dQ accumulator [B,Hq,Nq,d], each 256-byte
- * aligned. This is the largest need; attn_bwd_workspace_size_dt gives the
- * exact need of one dtype.
+ * [B,Hq,Nq] float32, 256 bytes for a work counter, and a float32 dQ
+ * accumulator [B,Hq,Nq,d], each 256-byte aligned. This is the largest
+ * need; attn_bwd_workspace_size_dt gives the exact need of one dtype.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d);
 
 /*
  * Bytes of device scratch attn_bwd (and attn_bwd_masked) use for dtype `dt`:
  * with dt = ATTN_BF16 and d = 128 only the row term D [B,Hq,Nq] float32
- * (256-byte aligned), because the dQ pass writes dQ directly; otherwise the
- * row term followed by the float32 dQ accumulator, as
+ * (256-byte aligned) and the 256-byte work counter of the dQ pass, which
+ * writes dQ directly; otherwise also the float32 dQ accumulator, as
  * attn_bwd_workspace_size. 0 for invalid arguments.
  */
 ATTN_API size_t attn_bwd_workspace_size_dt(int B, int Hq, int Hkv, int Nq, int Nk, int d,

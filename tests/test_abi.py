@@ -62,7 +62,9 @@ def _a256(x):
 def test_workspace_sizes(lib):
     B, H, N, d = 2, 16, 4096, 128
     rows = B * H * N
-    assert lib.attn_bwd_workspace_size(B, H, H, N, N, d) == _a256(rows * 4) + _a256(rows * d * 4)
+    # row term, 256 bytes for the dQ pass's work counter, float32 dQ accumulator
+    assert lib.attn_bwd_workspace_size(B, H, H, N, N, d) == \
+        _a256(rows * 4) + 256 + _a256(rows * d * 4)
     B, Hq, d, S = 64, 32, 128, 16
     n = B * Hq * S
     assert lib.attn_decode_workspace_size(B, Hq, d, S) == _a256(n * d * 4) + 2 * _a256(n * 4)
@@ -71,7 +73,7 @@ def test_workspace_sizes(lib):
     # per dtype: bf16 at d = 128 writes dQ directly and needs only the row term
     B, H, N = 2, 16, 4096
     rows = B * H * N
-    assert lib.attn_bwd_workspace_size_dt(B, H, H, N, N, 128, 1) == _a256(rows * 4)
+    assert lib.attn_bwd_workspace_size_dt(B, H, H, N, N, 128, 1) == _a256(rows * 4) + 256
     for d, dt in ((64, 1), (128, 0), (64, 0)):
         assert lib.attn_bwd_workspace_size_dt(B, H, H, N, N, d, dt) == \
             lib.attn_bwd_workspace_size(B, H, H, N, N, d)
