@@ -13,9 +13,13 @@
 // tiles that straddle a row's boundary are masked element by element.
 //
 // GB300 mapping (differs from the post's SRAM-only picture):
-//  * One CTA owns two 128-row query tiles of one head (256 rows) and streams
-//    128-key K/V tiles through a shared-memory ring filled by TMA
-//    (128-byte swizzle, zero fill past the end of the sequence).
+//  * One CTA owns two 128-row query tiles and streams 128-key K/V tiles
+//    through a shared-memory ring filled by TMA (128-byte swizzle, zero fill
+//    past the end of the sequence). Without grouped-query sharing the two
+//    tiles are consecutive rows of one head (256 rows); when two query heads
+//    share a KV head (Hq / Hkv even) they are the same 128 rows of two heads
+//    of the group, so every K/V tile loaded feeds both heads (the grouped
+//    heads of the KV-compression post's SnapKV code read one KV head).
 //  * S = Q Kᵀ and Õ += P̃ V run on tcgen05.mma (bf16 in, fp32 out) with both
 //    accumulators in tensor memory: S0, S1 (128 columns each) and Õ0, Õ1
 //    (d columns each).
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
               float* __restrict__ lse, int Hq, int Hkv, int Nq, int Nk, float scale,
-              MaskSpec mask, int n_qblk, int order_grp) {
+              MaskSpec mask, int n_qblk, int order_grp, int head_pairs) {
   using C = FwdCfg<D>;
   // Launched as a programmatic dependent of whatever precedes it in the
   // stream: the prologue (barriers, TMEM) overlaps that kernel's tail and
@@ -136,14 +140,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   __shared__ int4 keys_of_row[2 * kBM];   // each row's visible key intervals
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Heads in groups whose K/V fit in L2 together (causal; head-major
-  // otherwise); in a group the heaviest (latest) query blocks first.
-  int bh, rank;
-  grouped_tile_order(int(blockIdx.x), n_qblk, int(gridDim.x) / n_qblk, order_grp, bh, rank);
+  // Heads (or head pairs) in groups whose K/V fit in L2 together (causal;
+  // head-major otherwise); in a group the heaviest (latest) query blocks
+  // first. head_pairs: the CTA's tiles t = 0, 1 are rows [row0, row0 + 128)
+  // of query heads 2p and 2p + 1, which read the same KV head; otherwise
+  // rows row0 + 128·t of one head.
+  int hp, rank;
+  grouped_tile_order(int(blockIdx.x), n_qblk, int(gridDim.x) / n_qblk, order_grp, hp, rank);
   const int qblk = n_qblk - 1 - rank;
+  const int bh = head_pairs ? 2 * hp : hp;            // b·Hq + h of tile 0
   const int b = bh / Hq, h = bh % Hq;
   const int kvh = b * Hkv + h / (Hq / Hkv);
-  const int row0 = qblk * 2 * kBM;
+  const int row0 = qblk * (head_pairs ? kBM : 2 * kBM);
+  auto tile_row0 = [&](int t) { return head_pairs ? row0 : row0 + t * kBM; };
+  auto tile_bh = [&](int t) { return head_pairs ? bh + t : bh; };
 
   if (tid == 0) {
     bars.abort = 0;
@@ -183,7 +193,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     for (int t = 0; t < 2; ++t)
       for (int a = 0; a < C::kAtoms; ++a)
         tc::tma_load_3d(smem + C::kQOff + t * C::kTileBytes + a * (kBM * 128), &map_q, 64 * a,
-                        row0 + t * kBM, bh, &bars.q_full);
+                        tile_row0(t), tile_bh(t), &bars.q_full);
   }
   // The key tiles to visit. Without row ranges the plan follows from the
   // mask directly (no barrier: the loads start at once); with them every
@@ -197,16 +207,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     slots.init();
     slots.lo1 = 0;
     slots.hi1 = Nk - 1;
-    slots.last[0] = kv_tiles_for(row0, Nq, Nk, causal) * kBN - 1;
-    slots.last[1] = kv_tiles_for(row0 + kBM, Nq, Nk, causal) * kBN - 1;
+    slots.last[0] = kv_tiles_for(tile_row0(0), Nq, Nk, causal) * kBN - 1;
+    slots.last[1] = kv_tiles_for(tile_row0(1), Nq, Nk, causal) * kBN - 1;
   } else if (mask.row_kv_start == nullptr) {
-    slots = plan_slots_direct(mask, row0, kBM, 2, Nq, Nk);
+    slots = plan_slots_direct(mask, row0, kBM, head_pairs ? 1 : 2, Nq, Nk);
+    if (head_pairs) slots.last[1] = slots.last[0];   // the same rows
     if (tid == 0) bars.plan = slots;   // the producer thread reads it back below
   } else {
     if (warp >= 4) {
       const int t = (warp - 4) / 4;
       pdl_wait_primary();                                    // the ranges are inputs
-      const RowKeys rk = row_keys(mask, b, row0 + t * kBM + (warp % 4) * 32 + lane, Nq, Nk);
+      const RowKeys rk = row_keys(mask, b, tile_row0(t) + (warp % 4) * 32 + lane, Nq, Nk);
       store_row_keys(&keys_of_row[tid - 128], rk);
       plan_add_rows(&bars.plan, rk, t);
     }
@@ -341,7 +352,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     const int t = (warp - 4) / 4;                  // query tile of this warpgroup
     const int quarter = warp % 4;                  // TMEM lane quarter of this warp
     const int r = quarter * 32 + lane;             // row within the tile (TMEM lane)
-    const int row = row0 + t * kBM + r;            // query row
+    const int row = tile_row0(t) + r;              // query row
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t p_addr = tmem + lane_base + (t == 0 ? C::kColP0 : C::kColP1);
@@ -452,7 +463,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     // Epilogue: O = Õ / l -> bf16 -> swizzled smem (the dead Q tile) -> TMA
     // store. A tile that visited no key stores zeros (and LSE = -inf) once
     // its Q tile, the staging area, has landed.
-    const bool tile_rows = row0 + t * kBM < Nq;
+    const bool tile_rows = tile_row0(t) < Nq;
     if (ok && nt > 0)
       ok = mbar_wait_bounded(&bars.o_done[t], (nt - 1) & 1, abort_flag);
     else if (ok)
@@ -484,7 +495,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
         }
       }
       if (lse != nullptr && row < Nq)
-        lse[size_t(bh) * Nq + row] = l_run > 0.f ? (m_ref + __log2f(l_run)) * kLn2 : -INFINITY;
+        lse[size_t(tile_bh(t)) * Nq + row] = l_run > 0.f ? (m_ref + __log2f(l_run)) * kLn2 : -INFINITY;
       fence_proxy_async_smem();
     } else if (!ok) {
       if (lane == 0) attn_flag_error(kErrTimeout);
@@ -495,7 +506,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
     if (tile_rows && quarter == 0 && lane == 0 && !bars.abort) {
       uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
       for (int a = 0; a < C::kAtoms; ++a)
-        tma_store_3d(&map_o, stage + a * (kBM * 128), 64 * a, row0 + t * kBM, bh);
+        tma_store_3d(&map_o, stage + a * (kBM * 128), 64 * a, tile_row0(t), tile_bh(t));
       tma_store_commit_and_wait();
     }
   }
@@ -520,9 +531,15 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, kGeneral>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
-  const int n_qblk = (a.Nq + 2 * kBM - 1) / (2 * kBM);
-  const long blocks = long(n_qblk) * a.B * a.Hq;
+  // Two query heads per CTA when they share a KV head (Hq / Hkv even),
+  // else two row tiles of one head.
+  const int head_pairs = (a.Hq / a.Hkv) % 2 == 0 ? 1 : 0;
+  const int rows_per_cta = head_pairs ? kBM : 2 * kBM;
+  const int n_qblk = (a.Nq + rows_per_cta - 1) / rows_per_cta;
+  const long blocks = long(n_qblk) * a.B * (head_pairs ? a.Hq / 2 : a.Hq);
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
+  // K/V re-read per head (pair) within an L2 group: a pair shares one KV head
+  const long long kv_bytes = 4LL * a.Nk * D;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(blocks));
   cfg.blockDim = dim3(kThreads);
@@ -535,7 +552,7 @@ cudaError_t launch_fwd_tc_d(const FwdArgs& a) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, kGeneral>, mq, mk, mv, mo, a.lse, a.Hq, a.Hkv, a.Nq,
                             a.Nk, a.scale, a.mask, n_qblk,
-                            order_group(a.mask.varies(), 4LL * a.Nk * D));
+                            order_group(a.mask.varies(), kv_bytes), head_pairs);
 }
 
 }  // namespace

@@ -85,3 +85,17 @@ def test_causal_backward_workload_sampled_heads(ost):
         sl = lambda t: to_f64(t[b:b + 1, h:h + 1])
         ref = oracle.attention_bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["do"]), scale, True)
         _check_grads([sl(g) for g in got], ref, "bf16", (b, h))
+
+
+def test_gqa_backward_workload_sampled_kv_head(ost):
+    """B=2, Hq=16, Hkv=4, N=4096, d=128 causal bf16: dK and dV of a KV head
+    sum over its four query heads; the oracle computes one whole group (the
+    four query heads and their KV head) at each end of the batch."""
+    w = WORKLOADS["bwd_gqa_causal_n4096_d128"]
+    x, got, scale = _grads(ost, w)
+    for b, g in [(0, 0), (1, 3)]:
+        hs = slice(4 * g, 4 * g + 4)
+        qs = lambda t: to_f64(t[b:b + 1, hs])
+        ks = lambda t: to_f64(t[b:b + 1, g:g + 1])
+        ref = oracle.attention_bwd(qs(x["q"]), ks(x["k"]), ks(x["v"]), qs(x["do"]), scale, True)
+        _check_grads([qs(got[0]), ks(got[1]), ks(got[2])], ref, "bf16", (b, g))

@@ -71,6 +71,10 @@ SMALL = [
     (1, 1, 1, 1, 700, 128, "bf16", True),        # one query row sees every key
     (1, 2, 1, 640, 384, 64, "bf16", False),      # Nq > Nk, non-causal
     (1, 8, 2, 1000, 1000, 128, "bf16", True),
+    # d = 128 with an even group: one CTA runs the same rows of two query
+    # heads on shared K/V tiles; an odd group keeps two row tiles of a head
+    (2, 6, 3, 300, 300, 128, "bf16", False),
+    (1, 6, 2, 385, 385, 128, "bf16", True),
     (1, 2, 2, 129, 129, 64, "f32", True),
     (1, 3, 3, 70, 333, 128, "f32", False),
     (2, 4, 2, 200, 200, 128, "f32", True),
@@ -126,6 +130,23 @@ def test_causal_long_workload_sampled(ost):
     fixed = [0, 1, 127, 128, 129, 255, 4095, 4096, 8063, 8064, 8190, 8191]
     for b, h in [(0, 0), (1, 31), (0, 17), (1, 5)]:
         rows = np.unique(np.concatenate([fixed, rng.integers(0, w.Nq, 20)]))
+        o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, scale, True, b, h, rows)
+        _assert_o(o[b, h, rows], o_ref, "bf16", (b, h))
+        assert np.max(np.abs(lse[b, h, rows] - lse_ref)) <= 1e-3
+
+
+def test_gqa_long_workload_sampled(ost):
+    """B=2, Hq=32, Hkv=8, N=8192, d=128 causal bf16: two query heads of a
+    group share every K/V tile; sampled rows of heads at both ends of a
+    group and of the head axis, against the oracle row by row."""
+    w = WORKLOADS["fwd_gqa_causal_n8192_d128"]
+    x, o, lse, scale = _run(ost, w)
+    q, k, v = to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"])
+    o, lse = to_f64(o), to_f64(lse)
+    rng = np.random.default_rng(1)
+    fixed = [0, 1, 127, 128, 4095, 8190, 8191]
+    for b, h in [(0, 0), (0, 1), (1, 30), (1, 31), (0, 6)]:
+        rows = np.unique(np.concatenate([fixed, rng.integers(0, w.Nq, 12)]))
         o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, scale, True, b, h, rows)
         _assert_o(o[b, h, rows], o_ref, "bf16", (b, h))
         assert np.max(np.abs(lse[b, h, rows] - lse_ref)) <= 1e-3

@@ -81,6 +81,12 @@ WORKLOADS = {
     # The causal backward shape under a sliding window of 1024 keys.
     "bwd_swa_n4096_d128_w1024": Workload("bwd_swa_n4096_d128_w1024", "bwd", 2, 16, 16, 4096,
                                          4096, 128, "bf16", window_left=1023, window_right=0),
+    # The long-context forward and the causal backward with grouped-query
+    # heads: four query heads per KV head (8 KV heads of 32; 4 of 16).
+    "fwd_gqa_causal_n8192_d128": Workload("fwd_gqa_causal_n8192_d128", "fwd", 2, 32, 8, 8192,
+                                          8192, 128, "bf16", causal=True),
+    "bwd_gqa_causal_n4096_d128": Workload("bwd_gqa_causal_n4096_d128", "bwd", 2, 16, 4, 4096,
+                                          4096, 128, "bf16", causal=True),
     # Sparse-index decode as the ML notes' split-K kernel notes describe it:
     # T = 8 query tokens, 16 heads, 2048 listed rows per request, 32 splits;
     # 8 requests with caches of 16384 rows.
