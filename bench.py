@@ -3,9 +3,11 @@
 Default run (N=1): the long-context causal forward B=2, H=32, N=8192, d=128,
 bf16 (the line's top-level value), followed in the same process by the
 causal backward B=2, H=16, N=4096, d=128, the GQA split-KV decode (B=64,
-Hq=32, Hkv=8, L=4096, 16 splits) and the batched multi-head forward B=4,
-H=16, N=2048, d=64, each reported under ``workloads`` with its own value,
-roofline, CPU baseline, end-to-end rate and clocks. ``--workload`` picks the
+Hq=32, Hkv=8, L=4096, 16 splits), the batched multi-head forward B=4,
+H=16, N=2048, d=64, the forward and backward shapes with grouped-query heads
+(4 query heads per KV head) and the paged GQA decode (16-token pages, ragged
+lengths of mean 4096), each reported under ``workloads`` with its own
+value, roofline, CPU baseline, end-to-end rate and clocks. ``--workload`` picks the
 top-level workload and ``--extra`` the others (``--extra none``: only the
 top-level one). A step is one pass of the workload's hot path through the C
 ABI on inputs already resident in HBM; L2 is flushed (256 MiB write)
@@ -804,7 +806,8 @@ def run_gpu(args, w, extras):
 
 
 DEFAULT_WORKLOAD = "fwd_causal_n8192_d128"
-DEFAULT_EXTRA = "bwd_causal_n4096_d128,decode_gqa_l4096,fwd_mha_n2048_d64"
+DEFAULT_EXTRA = ("bwd_causal_n4096_d128,decode_gqa_l4096,fwd_mha_n2048_d64,"
+                 "fwd_gqa_causal_n8192_d128,bwd_gqa_causal_n4096_d128,decode_paged_gqa_l4096")
 
 
 def main():
@@ -819,7 +822,7 @@ def main():
                     help="comma-separated workloads timed after the top-level one and "
                          "reported under 'workloads' ('none': no others); default: "
                          f"{DEFAULT_EXTRA} when --workload is the default, else none")
-    ap.add_argument("--cpu-budget", type=float, default=10.0,
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
                     help="seconds of CPU oracle work for each cpu_baseline figure")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up and timed launches, no JSON line (for ncu captures)")
