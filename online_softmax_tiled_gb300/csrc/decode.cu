@@ -158,12 +158,17 @@ struct PagedKV {
   int rows;   // 1: sparse index list into the per-request cache
 };
 
-template <int D, int G, bool kPaged>
+// Where a chunk's keys come from: a contiguous cache, pages of a paged
+// cache (bulk copies by one thread), or a list of rows (every thread gathers).
+enum KeySource : int { kContiguous = 0, kPages = 1, kListedRows = 2 };
+
+template <int D, int G, int kSource>
 __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
                     int L, int S, int chunk, float scale, PagedKV pg, int rgroups) {
+  constexpr bool kPaged = kSource != kContiguous;   // keys reached through a table
   constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
   constexpr int kRowBytes = D * 2;
   constexpr int kStageBytes = kStageKeys * kRowBytes;
@@ -175,6 +180,9 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   __shared__ uint64_t full_bar[kStages];
   __shared__ int abort_flag;
   __shared__ int chunk_pages[kPaged ? kChunkPagesCached : 1];
+  constexpr int kPreStages = kSource == kPages ? 64 : 1;
+  __shared__ size_t stage_src[kPreStages][2];   // element offsets of a stage's one or two segments
+  __shared__ int stage_rows[kPreStages][2];
 
   // blockIdx.y = (KV head, group of G query rows); query row r of this CTA
   // is row b·Hq + blockIdx.y·G + r (Hq counts query rows: heads x tokens)
@@ -185,7 +193,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 
   // a sparse index list is gathered by every thread (cp.async), each
   // arriving on the stage barrier; otherwise thread 0 issues bulk copies
-  const bool gather_all = kPaged && pg.rows != 0;
+  constexpr bool gather_all = kSource == kListedRows;
   if (tid == 0) {
     abort_flag = 0;
     for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], gather_all ? kThreads : 1);
@@ -254,7 +262,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   const int nstages = (nkeys + kStageKeys - 1) / kStageKeys;
 
   // Element offset of key t of (b, g) in the K and V arrays.
-  const bool sparse = kPaged && pg.rows != 0;
+  constexpr bool sparse = kSource == kListedRows;
   const size_t head_off = kPaged && !sparse ? size_t(g) * pg.page_size * D
                                             : (size_t(b) * Hkv + g) * size_t(L) * D;
   const size_t page_elems = sparse ? size_t(D) : size_t(Hkv) * pg.page_size * D;   // gathers
@@ -278,13 +286,44 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     }
     cp_async_mbar_arrive(&full_bar[buf]);
   };
+  // Paged bulk copies: with pages of a multiple of 16 keys a 32-key stage
+  // touches at most two pages, and the source offsets of the first
+  // kPreStages stages are worked out here by all threads at once, so the
+  // copying thread spends a few instructions per stage (the per-stage
+  // barrier waits for it) instead of dividing by the page size.
+  const bool pre = kSource == kPages && pg.page_size % 16 == 0;
+  if (pre) {
+    for (int st = tid; st < min(nstages, kPreStages); st += kThreads) {
+      const int t0 = key_begin + st * kStageKeys;
+      const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+      const int in_page = t0 % pg.page_size;
+      const int seg = min(rows, pg.page_size - in_page);
+      stage_src[st][0] = head_off + size_t(page_of(t0)) * page_elems + size_t(in_page) * D;
+      stage_src[st][1] = seg < rows ? head_off + size_t(page_of(t0 + seg)) * page_elems : 0;
+      stage_rows[st][0] = seg;
+      stage_rows[st][1] = rows - seg;
+    }
+    __syncthreads();
+  }
   auto issue = [&](int st) {
     const int buf = st % kStages;
-    const int t0 = key_begin + st * kStageKeys;
-    const int rows = min(kStageKeys, nkeys - st * kStageKeys);
-    mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
-    if (kPaged) {
-      // one copy per page the stage touches (one when 32 | page_size)
+    if (kPaged && pre && st < kPreStages) {
+      const int r0 = stage_rows[st][0], r1 = stage_rows[st][1];
+      mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(r0 + r1) * kRowBytes);
+      const size_t o0 = stage_src[st][0];
+      bulk_g2s(sK + buf * kStageBytes, k + o0, uint32_t(r0) * kRowBytes, &full_bar[buf]);
+      bulk_g2s(sV + buf * kStageBytes, v + o0, uint32_t(r0) * kRowBytes, &full_bar[buf]);
+      if (r1 > 0) {
+        const size_t o1 = stage_src[st][1];
+        const uint32_t dst = buf * kStageBytes + r0 * kRowBytes;
+        bulk_g2s(sK + dst, k + o1, uint32_t(r1) * kRowBytes, &full_bar[buf]);
+        bulk_g2s(sV + dst, v + o1, uint32_t(r1) * kRowBytes, &full_bar[buf]);
+      }
+    } else if (kPaged) {
+      const int t0 = key_begin + st * kStageKeys;
+      const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+      mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
+      // one copy per page the stage touches
       for (int t = t0, r = 0; r < rows;) {
         const int in_page = t % pg.page_size;
         const int seg = min(rows - r, pg.page_size - in_page);
@@ -296,6 +335,9 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
         r += seg;
       }
     } else {
+      const int t0 = key_begin + st * kStageKeys;
+      const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+      mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
       const size_t off = head_off + size_t(t0) * D;
       bulk_g2s(sK + buf * kStageBytes, k + off, uint32_t(rows) * kRowBytes, &full_bar[buf]);
       bulk_g2s(sV + buf * kStageBytes, v + off, uint32_t(rows) * kRowBytes, &full_bar[buf]);
@@ -531,10 +573,10 @@ merge_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
   if (lse != nullptr && lane == 0) lse[row] = empty ? -INFINITY : mx + logf(l);
 }
 
-template <int D, int G, bool kPaged>
+template <int D, int G, int kSource>
 cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
   const size_t smem = decode_smem_bytes<D, G>();
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, kPaged>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, kSource>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -549,7 +591,7 @@ cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
   cfg.numAttrs = 1;
   const PagedKV pg{a.block_table, a.seq_lens, a.num_pages, a.page_size, a.max_pages,
                    a.sparse ? 1 : 0};
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, kPaged>,
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, kSource>,
                             static_cast<const __nv_bfloat16*>(a.q),
                             static_cast<const __nv_bfloat16*>(a.k),
                             static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part,
@@ -561,7 +603,7 @@ cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
 // of them for single-token decode; with several tokens at most 4 at d = 128
 // and 8 at d = 64, the register budget of one CTA) and the rest go to
 // further CTAs over the same keys.
-template <int D, bool kPaged>
+template <int D, int kSource>
 cudaError_t launch_split_d(const DecodeArgs& a) {
   const int rows = (a.Hq / a.Hkv) * a.T;
   int G = rows;
@@ -572,10 +614,10 @@ cudaError_t launch_split_d(const DecodeArgs& a) {
   }
   const int rgroups = rows / G;
   switch (G) {
-    case 1: return launch_split_t<D, 1, kPaged>(a, rgroups);
-    case 2: return launch_split_t<D, 2, kPaged>(a, rgroups);
-    case 4: return launch_split_t<D, 4, kPaged>(a, rgroups);
-    case 8: return launch_split_t<D, 8, kPaged>(a, rgroups);
+    case 1: return launch_split_t<D, 1, kSource>(a, rgroups);
+    case 2: return launch_split_t<D, 2, kSource>(a, rgroups);
+    case 4: return launch_split_t<D, 4, kSource>(a, rgroups);
+    case 8: return launch_split_t<D, 8, kSource>(a, rgroups);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -583,9 +625,11 @@ cudaError_t launch_split_d(const DecodeArgs& a) {
 }  // namespace
 
 cudaError_t launch_decode_split(const DecodeArgs& a) {
+  if (a.block_table != nullptr && a.sparse)
+    return a.d == 64 ? launch_split_d<64, kListedRows>(a) : launch_split_d<128, kListedRows>(a);
   if (a.block_table != nullptr)
-    return a.d == 64 ? launch_split_d<64, true>(a) : launch_split_d<128, true>(a);
-  return a.d == 64 ? launch_split_d<64, false>(a) : launch_split_d<128, false>(a);
+    return a.d == 64 ? launch_split_d<64, kPages>(a) : launch_split_d<128, kPages>(a);
+  return a.d == 64 ? launch_split_d<64, kContiguous>(a) : launch_split_d<128, kContiguous>(a);
 }
 
 cudaError_t launch_merge(const MergeArgs& a) {
