@@ -37,11 +37,18 @@
 // touches (rows are 128 or 256 bytes, so every row start is 16-byte
 // aligned); chunks start on multiples of 32 keys, so with 32 | page_size
 // that is one copy per tensor, as for a contiguous cache.
+//
+// Sparse-index decode (ML notes, sparse-attention split-K notes: the kernel
+// gathers the listed KV rows into shared memory tile by tile): the same
+// kernel over one list of cache rows per request, each 32-row stage filled
+// by tile::gather4 tensor copies of four listed rows each (a 2-D view of the
+// cache, one row per box), issued by 16 lanes of warp 0 at once.
 
 #include <mutex>
 
 #include "common.cuh"
 #include "launchers.h"
+#include "tma_host.h"
 
 namespace attn {
 
@@ -159,15 +166,30 @@ struct PagedKV {
 };
 
 // Where a chunk's keys come from: a contiguous cache, pages of a paged
-// cache (bulk copies by one thread), or a list of rows (every thread gathers).
+// cache (bulk copies by one thread), or a list of rows (tile::gather4 copies
+// of four rows each, issued by the lanes of warp 0).
 enum KeySource : int { kContiguous = 0, kPages = 1, kListedRows = 2 };
+
+// Four rows of a 2-D tensor map (box: one row of `cols` elements), given by
+// their row coordinates, into consecutive rows at smem_dst (tile::gather4).
+ATTN_DEVINL void tma_gather4(void* smem_dst, const CUtensorMap* map, int r0, int r1, int r2,
+                             int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(r0), "r"(r1),
+        "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
 
 template <int D, int G, int kSource>
 __global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
-                    int L, int S, int chunk, float scale, PagedKV pg, int rgroups) {
+                    int L, int S, int chunk, float scale, PagedKV pg, int rgroups,
+                    const __grid_constant__ CUtensorMap map_k_rows,
+                    const __grid_constant__ CUtensorMap map_v_rows) {
   constexpr bool kPaged = kSource != kContiguous;   // keys reached through a table
   constexpr int NV = D / 64;                       // 16-byte pieces per lane per row
   constexpr int kRowBytes = D * 2;
@@ -191,12 +213,11 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;
 
-  // a sparse index list is gathered by every thread (cp.async), each
-  // arriving on the stage barrier; otherwise thread 0 issues bulk copies
-  constexpr bool gather_all = kSource == kListedRows;
+  // one arrival per stage barrier (the expected-bytes arrival of the
+  // thread that issues the stage's copies)
   if (tid == 0) {
     abort_flag = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], gather_all ? kThreads : 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
     fence_barrier_init();
   }
   // Launched as a programmatic dependent: every global access of this grid
@@ -265,26 +286,10 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   constexpr bool sparse = kSource == kListedRows;
   const size_t head_off = kPaged && !sparse ? size_t(g) * pg.page_size * D
                                             : (size_t(b) * Hkv + g) * size_t(L) * D;
-  const size_t page_elems = sparse ? size_t(D) : size_t(Hkv) * pg.page_size * D;   // gathers
+  const size_t page_elems = sparse ? size_t(D) : size_t(Hkv) * pg.page_size * D;
   auto page_of = [&](int t) {
     const int i = t / pg.page_size - p_first;
     return i < kChunkPagesCached ? chunk_pages[i] : table_row[t / pg.page_size];
-  };
-  // Sparse list (all threads): 16-byte pieces, consecutive threads along a
-  // row, so a listed row is one coalesced 128- or 256-byte read per tensor.
-  auto gather = [&](int st) {
-    constexpr int kPieces = kRowBytes / 16;
-    const int buf = st % kStages;
-    const int t0 = key_begin + st * kStageKeys;
-    const int rows = min(kStageKeys, nkeys - st * kStageKeys);
-    for (int p = tid; p < rows * 2 * kPieces; p += kThreads) {
-      const int r = p / (2 * kPieces), rem = p % (2 * kPieces);
-      const int tensor = rem / kPieces, piece = rem % kPieces;
-      const size_t off = head_off + size_t(page_of(t0 + r)) * page_elems;
-      const uint8_t* src = reinterpret_cast<const uint8_t*>((tensor ? v : k) + off) + piece * 16;
-      cp_async16((tensor ? sV : sK) + buf * kStageBytes + r * kRowBytes + piece * 16, src);
-    }
-    cp_async_mbar_arrive(&full_bar[buf]);
   };
   // Paged bulk copies: with pages of a multiple of 16 keys a 32-key stage
   // touches at most two pages, and the source offsets of the first
@@ -307,7 +312,30 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   }
   auto issue = [&](int st) {
     const int buf = st % kStages;
-    if (kPaged && pre && st < kPreStages) {
+    if (kSource == kListedRows) {
+      // listed rows (every lane of warp 0): four rows per gather4 copy, lane
+      // o < 8 copies K rows 4o .. 4o + 3 of the stage and lane 8 + o the same
+      // V rows; a last copy of fewer rows repeats the stage's last row into
+      // slots nobody reads
+      const int e0 = st * kStageKeys;
+      const int rows = min(kStageKeys, nkeys - e0);
+      const int nops = (rows + 3) / 4;
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(nops) * 4 * kRowBytes);
+      __syncwarp();
+      const int o = lane & 7;
+      if (lane < 16 && o < nops) {
+        const int rbase = (b * Hkv + g) * L;   // row of key 0 of (request, KV head)
+        int r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          r[i] = rbase + page_of(key_begin + min(e0 + 4 * o + i, nkeys - 1));
+        const uint32_t dst = buf * kStageBytes + 4 * o * kRowBytes;
+        if (lane < 8)
+          tma_gather4(sK + dst, &map_k_rows, r[0], r[1], r[2], r[3], &full_bar[buf]);
+        else
+          tma_gather4(sV + dst, &map_v_rows, r[0], r[1], r[2], r[3], &full_bar[buf]);
+      }
+    } else if (kPaged && pre && st < kPreStages) {
       const int r0 = stage_rows[st][0], r1 = stage_rows[st][1];
       mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(r0 + r1) * kRowBytes);
       const size_t o0 = stage_src[st][0];
@@ -343,12 +371,11 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
       bulk_g2s(sV + buf * kStageBytes, v + off, uint32_t(rows) * kRowBytes, &full_bar[buf]);
     }
   };
-  int issued = 0;  // meaningful in thread 0 only (every thread when gathering)
-  if (gather_all) {
-    for (; issued < min(kStages, nstages); ++issued) gather(issued);
-  } else if (tid == 0) {
+  int issued = 0;  // meaningful in the issuing thread (warp) only
+  // Thread 0 issues the copies; for listed rows the whole of warp 0.
+  const bool issuer = kSource == kListedRows ? warp == 0 : tid == 0;
+  if (issuer)
     for (; issued < min(kStages, nstages); ++issued) issue(issued);
-  }
 
   // Query slice of this lane for all G heads, pre-scaled into log2 units,
   // as pairs of consecutive dimensions (packed f32x2 arithmetic).
@@ -388,10 +415,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     // stage st-1 is free once every thread has arrived here.
     if (__syncthreads_or(fail)) {
       // Let copies already issued land before shared memory goes away.
-      if (gather_all) {
-        cp_async_wait_all();
-        if (tid == 0) attn_flag_error(kErrTimeout);
-      } else if (tid == 0) {
+      if (tid == 0) {
         attn_flag_error(kErrTimeout);
         for (int t = st; t < issued; ++t)
           mbar_wait_bounded(&full_bar[t % kStages], (t / kStages) & 1, nullptr);
@@ -399,11 +423,7 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
       ok = false;
       break;
     }
-    if (gather_all) {
-      if (issued < nstages && st >= 1) gather(issued++);
-    } else if (tid == 0 && issued < nstages && st >= 1) {
-      issue(issued++);
-    }
+    if (issuer && issued < nstages && st >= 1) issue(issued++);
     const int rows = min(kStageKeys, nkeys - st * kStageKeys);
     const uint8_t* kb = sK + buf * kStageBytes;
     const uint8_t* vb = sV + buf * kStageBytes;
@@ -591,12 +611,19 @@ cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
   cfg.numAttrs = 1;
   const PagedKV pg{a.block_table, a.seq_lens, a.num_pages, a.page_size, a.max_pages,
                    a.sparse ? 1 : 0};
+  // listed rows: the caches as [B·Hkv·L rows][d] for row gathers
+  CUtensorMap mk{}, mv{};
+  if (kSource == kListedRows) {
+    const uint64_t rows = uint64_t(a.B) * a.Hkv * a.L;
+    if (!make_map_bf16_rows(&mk, a.k, D, rows) || !make_map_bf16_rows(&mv, a.v, D, rows))
+      return cudaErrorInvalidValue;
+  }
   return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, kSource>,
                             static_cast<const __nv_bfloat16*>(a.q),
                             static_cast<const __nv_bfloat16*>(a.k),
                             static_cast<const __nv_bfloat16*>(a.v), a.o_part, a.m_part, a.l_part,
                             a.Hq * a.T, a.Hkv, a.L, a.num_splits, decode_chunk(a), a.scale, pg,
-                            rgroups);
+                            rgroups, mk, mv);
 }
 
 // Query rows per KV head: (Hq / Hkv) x T. One CTA takes G of them (G = all
