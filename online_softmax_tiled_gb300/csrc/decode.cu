@@ -336,33 +336,38 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
           tma_gather4(sV + dst, &map_v_rows, r[0], r[1], r[2], r[3], &full_bar[buf]);
       }
     } else if (kPaged && pre && st < kPreStages) {
+      // (every lane of warp 0) one copy per lane: lane 2·seg + tensor copies
+      // segment seg of K (tensor 0) or V (tensor 1)
       const int r0 = stage_rows[st][0], r1 = stage_rows[st][1];
-      mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(r0 + r1) * kRowBytes);
-      const size_t o0 = stage_src[st][0];
-      bulk_g2s(sK + buf * kStageBytes, k + o0, uint32_t(r0) * kRowBytes, &full_bar[buf]);
-      bulk_g2s(sV + buf * kStageBytes, v + o0, uint32_t(r0) * kRowBytes, &full_bar[buf]);
-      if (r1 > 0) {
-        const size_t o1 = stage_src[st][1];
-        const uint32_t dst = buf * kStageBytes + r0 * kRowBytes;
-        bulk_g2s(sK + dst, k + o1, uint32_t(r1) * kRowBytes, &full_bar[buf]);
-        bulk_g2s(sV + dst, v + o1, uint32_t(r1) * kRowBytes, &full_bar[buf]);
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(r0 + r1) * kRowBytes);
+      __syncwarp();
+      if (lane < (r1 > 0 ? 4 : 2)) {
+        const int seg = lane >> 1;
+        const size_t o = stage_src[st][seg];
+        const uint32_t dst = buf * kStageBytes + (seg ? r0 : 0) * kRowBytes;
+        const uint32_t bytes = uint32_t(seg ? r1 : r0) * kRowBytes;
+        bulk_g2s(((lane & 1) ? sV : sK) + dst, ((lane & 1) ? v : k) + o, bytes, &full_bar[buf]);
       }
     } else if (kPaged) {
-      const int t0 = key_begin + st * kStageKeys;
-      const int rows = min(kStageKeys, nkeys - st * kStageKeys);
-      mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
-      // one copy per page the stage touches
-      for (int t = t0, r = 0; r < rows;) {
-        const int in_page = t % pg.page_size;
-        const int seg = min(rows - r, pg.page_size - in_page);
-        const size_t off = head_off + size_t(page_of(t)) * page_elems + size_t(in_page) * D;
-        const uint32_t dst = buf * kStageBytes + r * kRowBytes;
-        bulk_g2s(sK + dst, k + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
-        bulk_g2s(sV + dst, v + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
-        t += seg;
-        r += seg;
+      // other page sizes, later stages: lane 0 alone, one copy per page the
+      // stage touches
+      if (lane == 0) {
+        const int t0 = key_begin + st * kStageKeys;
+        const int rows = min(kStageKeys, nkeys - st * kStageKeys);
+        mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
+        for (int t = t0, r = 0; r < rows;) {
+          const int in_page = t % pg.page_size;
+          const int seg = min(rows - r, pg.page_size - in_page);
+          const size_t off = head_off + size_t(page_of(t)) * page_elems + size_t(in_page) * D;
+          const uint32_t dst = buf * kStageBytes + r * kRowBytes;
+          bulk_g2s(sK + dst, k + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
+          bulk_g2s(sV + dst, v + off, uint32_t(seg) * kRowBytes, &full_bar[buf]);
+          t += seg;
+          r += seg;
+        }
       }
     } else {
+      // contiguous cache: thread 0 alone (the only issuer)
       const int t0 = key_begin + st * kStageKeys;
       const int rows = min(kStageKeys, nkeys - st * kStageKeys);
       mbar_arrive_expect_tx(&full_bar[buf], 2 * uint32_t(rows) * kRowBytes);
@@ -372,8 +377,9 @@ decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     }
   };
   int issued = 0;  // meaningful in the issuing thread (warp) only
-  // Thread 0 issues the copies; for listed rows the whole of warp 0.
-  const bool issuer = kSource == kListedRows ? warp == 0 : tid == 0;
+  // Thread 0 issues the copies of a contiguous cache; for pages and listed
+  // rows the lanes of warp 0 share them.
+  const bool issuer = kSource == kContiguous ? tid == 0 : warp == 0;
   if (issuer)
     for (; issued < min(kStages, nstages); ++issued) issue(issued);
 
