@@ -84,3 +84,12 @@ def test_merge_kernel_permuted_and_empty_splits(ost, out_dtype):
     assert np.isneginf(got_lse[5]) and np.all(to_f64(o)[5] == 0)
     fin = np.isfinite(lse_ref)
     assert np.max(np.abs(got_lse[fin] - lse_ref[fin])) <= 1e-5
+
+
+def test_long_cache(ost):
+    """One request with a 131072-key cache, 64 splits of 2048 keys, GQA 4:1,
+    and a cache whose length is not a multiple of the split count."""
+    _check(ost, Workload("long", "decode", 1, 8, 2, 1, 131072, 128, "bf16", num_splits=64,
+                         seed=81))
+    _check(ost, Workload("long_ragged", "decode", 2, 4, 1, 1, 100003, 64, "bf16",
+                         num_splits=37, seed=82))

@@ -150,3 +150,19 @@ def test_gqa_long_workload_sampled(ost):
         o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, scale, True, b, h, rows)
         _assert_o(o[b, h, rows], o_ref, "bf16", (b, h))
         assert np.max(np.abs(lse[b, h, rows] - lse_ref)) <= 1e-3
+
+
+def test_long_sequence_sampled_rows(ost):
+    """N = 32768 causal at d = 128 (one batch entry, two heads), and a
+    non-causal N = 16384 at d = 64: the longest key ranges the tests reach,
+    sampled rows (each row is independent) against the oracle."""
+    for w in (Workload("long128", "fwd", 1, 2, 2, 32768, 32768, 128, "bf16", True, seed=71),
+              Workload("long64", "fwd", 1, 2, 1, 16384, 16384, 64, "bf16", False, seed=72)):
+        x, o, lse, scale = _run(ost, w)
+        q, k, v = to_f64(x["q"]), to_f64(x["k"]), to_f64(x["v"])
+        o, lse = to_f64(o), to_f64(lse)
+        rows = np.array([0, 1, 127, 128, 4096, w.Nq // 2, w.Nq - 129, w.Nq - 2, w.Nq - 1])
+        for h in range(w.Hq):
+            o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, scale, w.causal, 0, h, rows)
+            _assert_o(o[0, h, rows], o_ref, "bf16", (w.name, h))
+            assert np.max(np.abs(lse[0, h, rows] - lse_ref)) <= 1e-3
