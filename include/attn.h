@@ -249,10 +249,14 @@ ATTN_API attn_status attn_decode_splitkv(const void* q, const void* k_cache, con
  * Hq/Hkv <= 8.
  * A request with n_b = 0 gets O = 0, LSE = -inf. Chunks have one length for
  * all requests, c = ceil(max_pages_per_seq * page_size / num_splits)
- * rounded up to a multiple of 32 keys; request b uses its own number of
- * splits, ceil(n_b / c) <= num_splits, split s covering keys
+ * rounded up to a multiple of 32 keys, then doubled while the grid keeps
+ * at least 8 CTAs per resident CTA slot of the device (B * Hkv *
+ * ceil(capacity / c) CTAs; every CTA pays the same start, so a large batch
+ * runs fewer, longer chunks); request b uses its own number of splits,
+ * ceil(n_b / c) <= num_splits, split s covering keys
  * [s*c, min((s+1)*c, n_b)), so every split carries about the same work
- * whatever the mix of lengths.
+ * whatever the mix of lengths. num_splits is thus the most splits a request
+ * uses, and the partials keep that stride.
  * Device-side checks: a length outside [0, max_pages_per_seq*page_size] or
  * a page index outside [0, num_pages) is never dereferenced; the request
  * (for a bad length) or the split holding the bad index gets no keys, and

@@ -27,7 +27,8 @@
 // through a page table): the same kernel with request b's length read from
 // seq_lens[b] and key t read from page block_table[b][t / page_size].
 // Chunks have one length c for all requests (the table's capacity over the
-// split count, rounded up to 32 keys), so request b uses its own number of
+// split count, rounded up to 32 keys, doubled while the grid keeps eight
+// CTAs per resident slot: decode_chunk), so request b uses its own number of
 // splits, ceil(n_b / c), every non-empty chunk carries about the same work
 // and the CTAs of chunks past a request's end return at once (the merge
 // reads only a request's own chunks). A CTA fetches its request's length and
@@ -606,7 +607,7 @@ cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.num_splits, a.Hkv * rgroups, a.B);
+  cfg.gridDim = dim3(decode_grid_splits(a), a.Hkv * rgroups, a.B);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;

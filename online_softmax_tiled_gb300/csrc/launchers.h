@@ -104,18 +104,59 @@ struct MergeArgs {
   int Hq = 1, len = 0, max_len = 0, chunk = 0;
 };
 
+// Streaming multiprocessors of the current device (cached per device); 0 if
+// it cannot be read.
+inline int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // Keys per decode chunk: ceil(L / S) for a contiguous cache; for a paged
 // cache one length for all requests, the table's capacity over S rounded up
 // to whole 32-key stages, so request b uses ceil(n_b / chunk) <= S chunks.
 // A sparse index list has chunks of at least 128 entries (four 32-entry
 // stages): smaller ones leave each CTA too little work to cover its start.
+//
+// Paged caches: every CTA pays the same start whatever its chunk (its
+// request's length and table entries come back before its first copy can be
+// issued, and a chunk past the request's end still pays that round trip to
+// learn it is empty), so the chunk doubles while the grid keeps at least
+// kDecodeWaves CTAs per resident slot: fewer, longer chunks cover the same
+// keys with fewer starts, and enough CTAs stay to balance the last wave.
+constexpr int kDecodeWaves = 8;
 inline int decode_chunk(const DecodeArgs& a) {
   if (a.block_table == nullptr) return (a.L + a.num_splits - 1) / a.num_splits;
   const long long cap = 1LL * a.max_pages * a.page_size;
   long long c = (cap + a.num_splits - 1) / a.num_splits;
   c = (c + 31) / 32 * 32;
-  if (a.sparse && c < 128) c = 128;
+  if (a.sparse) return int(c < 128 ? 128 : c);
+  // resident CTAs per SM of the split kernel: 3 with up to 4 query rows per
+  // KV head, 2 with 8 (register-bound)
+  const long long slots = 1LL * device_sm_count() * (a.Hq <= 4 * a.Hkv ? 3 : 2);
+  if (slots <= 0) return int(c);
+  while (2 * c < (1LL << 30)) {
+    const long long splits = (cap + c - 1) / c, splits2 = (cap + 2 * c - 1) / (2 * c);
+    if (splits2 == splits || 1LL * a.B * a.Hkv * splits2 < kDecodeWaves * slots) break;
+    c *= 2;
+  }
   return int(c);
+}
+
+// Chunk indices the split grid covers: the paged cache's ceil(capacity /
+// chunk) (<= S; the partials keep the stride S), otherwise S.
+inline int decode_grid_splits(const DecodeArgs& a) {
+  if (a.block_table == nullptr || a.sparse) return a.num_splits;
+  const long long cap = 1LL * a.max_pages * a.page_size;
+  const long long c = decode_chunk(a);
+  const long long n = (cap + c - 1) / c;
+  return int(n < a.num_splits ? n : a.num_splits);
 }
 
 // The merge that completes a decode call.
@@ -141,20 +182,6 @@ inline int order_group(bool causal, long long bytes_per_head, long long budget =
 
 // Workspace carving (bytes, 256-aligned sections).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Streaming multiprocessors of the current device (cached per device); 0 if
-// it cannot be read.
-inline int device_sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
 
 // The bf16 d = 128 backward without a general mask runs its dQ pass as a
 // persistent grid that takes work from a counter in the workspace.

@@ -55,6 +55,17 @@ def test_paged_gqa_workload_full(ost):
     _check(ost, WORKLOADS["decode_paged_gqa_l4096"])
 
 
+def test_large_batch_long_chunks_at_their_boundaries(ost):
+    """A batch large enough for the split grid to take chunks longer than
+    capacity / num_splits (64 requests x 8 KV heads: 512-key chunks double
+    to 1024 on a full device), with lengths on either side of the chunk
+    boundaries, at the table's capacity, and empty: every output row."""
+    w = Workload("paged_long_chunks", "decode_paged", 64, 32, 8, 1, 4096, 128, "bf16",
+                 num_splits=16, seed=91, page_size=16)
+    pattern = [1, 511, 512, 513, 1023, 1024, 1025, 2047, 2048, 4097, 8191, 8192, 0, 3000, 32, 33]
+    _check(ost, w, [pattern[i % len(pattern)] for i in range(w.B)])
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,d,page,S,lens", [
     (4, 8, 2, 128, 32, 4, [0, 1, 31, 33]),         # an empty request, one key, ragged tails
     (3, 16, 2, 64, 16, 7, [300, 5, 1000]),         # group of 8, pages of 16 keys
