@@ -156,7 +156,7 @@ def rate(units, seconds, unit):
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms; the samples whose timestamps fall in
+    """nvidia-smi sampled every 20 ms; the samples whose timestamps fall in
     the timed window (or, for a window shorter than the period, the ones
     next to it) give the reported clocks."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -169,7 +169,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
