@@ -251,7 +251,8 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
-  if (num_splits > 65535 || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  // (eight query heads per KV head run as two CTAs of four: grid rows Hkv·2)
+  if (num_splits > 65535 || B > 65535 || 1LL * Hkv * G > 65535) return ATTN_ERR_UNSUPPORTED;
   // work items (request, KV head, chunk) are numbered in 32 bits
   if (1LL * B * Hkv * num_splits > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
@@ -283,7 +284,8 @@ attn_status attn_decode_paged(const void* q, const void* k_pages, const void* v_
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
-  if (num_splits > 65535 || B > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  // (eight query heads per KV head run as two CTAs of four: grid rows Hkv·2)
+  if (num_splits > 65535 || B > 65535 || 1LL * Hkv * G > 65535) return ATTN_ERR_UNSUPPORTED;
   // work items (request, KV head, chunk) are numbered in 32 bits
   if (1LL * B * Hkv * num_splits > (1LL << 30)) return ATTN_ERR_UNSUPPORTED;
   // key positions and page row offsets are 32-bit inside the kernel

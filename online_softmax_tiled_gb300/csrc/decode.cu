@@ -11,8 +11,9 @@
 //
 // Split kernel. Decode is bound by reading the KV cache once (about 4 flops
 // per byte), so it runs on the FMA pipes, not the tensor cores. One CTA owns
-// (request b, KV head g, chunk s) and all G = Hq/Hkv query heads that share
-// that KV head, so every K/V byte is read from HBM exactly once. K and V
+// (request b, KV head g, chunk s) and the G = Hq/Hkv query heads that share
+// that KV head (up to four; with eight, two CTAs of four read the same
+// keys), so every K/V byte is read from HBM once per CTA group. K and V
 // rows of the chunk stream through a 4-stage shared-memory ring filled by
 // bulk asynchronous copies (each stage is a contiguous run of rows, so one
 // copy per tensor per stage). Eight consecutive lanes own one key: lane
@@ -184,7 +185,7 @@ ATTN_DEVINL void tma_gather4(void* smem_dst, const CUtensorMap* map, int r0, int
 }
 
 template <int D, int G, int kSource>
-__global__ void __launch_bounds__(kThreads, (G <= 4 ? 3 : 1))
+__global__ void __launch_bounds__(kThreads, 3)
 decode_split_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const __nv_bfloat16* __restrict__ v, float* __restrict__ o_part,
                     float* __restrict__ m_part, float* __restrict__ l_part, int Hq, int Hkv,
@@ -633,25 +634,21 @@ cudaError_t launch_split_t(const DecodeArgs& a, int rgroups) {
                             rgroups, mk, mv);
 }
 
-// Query rows per KV head: (Hq / Hkv) x T. One CTA takes G of them (G = all
-// of them for single-token decode; with several tokens at most 4 at d = 128
-// and 8 at d = 64, the register budget of one CTA) and the rest go to
-// further CTAs over the same keys.
+// Query rows per KV head: (Hq / Hkv) x T. One CTA takes G of them, at most
+// 4, and the rest go to further CTAs over the same keys. Eight rows per CTA
+// need 200-255 registers a thread (spilling at d = 128) and leave one or two
+// CTAs per SM: two CTAs of four rows each read the keys twice and still run
+// 1.6x (d = 128) and 1.1x (d = 64) faster than one CTA of eight.
 template <int D, int kSource>
 cudaError_t launch_split_d(const DecodeArgs& a) {
   const int rows = (a.Hq / a.Hkv) * a.T;
-  int G = rows;
-  if (a.T > 1) {
-    const int cap = D == 128 ? 4 : 8;
-    G = 1;
-    while (G * 2 <= cap && rows % (G * 2) == 0) G *= 2;
-  }
+  int G = 1;
+  while (G * 2 <= 4 && rows % (G * 2) == 0) G *= 2;
   const int rgroups = rows / G;
   switch (G) {
     case 1: return launch_split_t<D, 1, kSource>(a, rgroups);
     case 2: return launch_split_t<D, 2, kSource>(a, rgroups);
     case 4: return launch_split_t<D, 4, kSource>(a, rgroups);
-    case 8: return launch_split_t<D, 8, kSource>(a, rgroups);
     default: return cudaErrorInvalidValue;
   }
 }

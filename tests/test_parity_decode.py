@@ -41,11 +41,12 @@ def test_gqa_decode_workload_full(ost):
 @pytest.mark.parametrize("B,Hq,Hkv,L,d,S", [
     (2, 8, 2, 300, 128, 7),
     (1, 4, 4, 50, 64, 16),
-    (3, 16, 2, 1000, 128, 3),     # group of 8
+    (3, 16, 2, 1000, 128, 3),     # group of 8 (two CTAs of four rows)
     (2, 4, 2, 5, 128, 16),        # splits 5..15 are empty
     (1, 2, 1, 1, 64, 1),
     (1, 8, 8, 4096, 128, 1),      # one split covers everything
     (4, 32, 8, 777, 64, 5),
+    (2, 16, 2, 513, 64, 4),       # group of 8 at d = 64 (two CTAs of four rows)
 ])
 def test_small_shapes(ost, B, Hq, Hkv, L, d, S):
     _check(ost, Workload("small", "decode", B, Hq, Hkv, 1, L, d, "bf16", num_splits=S, seed=L + S))
