@@ -69,6 +69,7 @@ def test_large_batch_long_chunks_at_their_boundaries(ost):
 @pytest.mark.parametrize("B,Hq,Hkv,d,page,S,lens", [
     (4, 8, 2, 128, 32, 4, [0, 1, 31, 33]),         # an empty request, one key, ragged tails
     (3, 16, 2, 64, 16, 7, [300, 5, 1000]),         # group of 8, pages of 16 keys
+    (2, 16, 2, 128, 16, 5, [777, 40]),             # group of 8 at d = 128 (a CTA pair)
     (2, 4, 4, 128, 64, 16, [2048, 100]),           # MHA; the short request leaves splits empty
     (2, 8, 1, 128, 48, 5, [777, 96]),              # stages straddle 48-key pages
     (2, 8, 2, 64, 1, 3, [70, 33]),                 # one key per page
