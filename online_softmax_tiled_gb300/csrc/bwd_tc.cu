@@ -71,7 +71,7 @@ struct BwdCfg {
   // without swizzle. d = 64: the softmax reads -LSE·log2e and -D from
   // per-stage float vectors.
   static constexpr bool kAugTerms = !kFusedDq;
-  static constexpr int kAugTile = BQ * 32 * 2;                      // B: 4 core-matrix columns
+  static constexpr int kAugTile = 2 * BQ * 16 * 2;                  // B: 2·BQ rows x 16
   static constexpr int kOffOnes = kOffP + kPsBufs * kPsTile;        // A: 128 x 16 ones
   static constexpr int kOffAug = kOffOnes + (kAugTerms ? kBK * 16 * 2 : 0);   // [stage] B
   static constexpr int kOffVec = kOffAug + (kAugTerms ? kQStages * kAugTile : 0);
@@ -161,17 +161,18 @@ ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* do
     tc::mma_ss_warp(tmem + C::col_dp(b), v_km + ka, dd + qb, idesc_sdp, kk > 0);
   }
   if (C::kAugTerms) {
-    // Sᵀ += 1 · (-LSE/scale parts), dPᵀ += 1 · (-D parts): one K = 16 step
-    // each, so Pᵀ = exp2(Sᵀ·scale·log2e) and dSᵀ = Pᵀ ∘ dPᵀ need no
-    // per-column loads. Layout: core matrices of 8 rows x 16 bytes; A has
-    // 2 along K (lbo 128) and 8-row groups every 256 bytes; B has 4 along K
-    // (lbo 128: -LSE parts in the first two, -D parts in the last two) and
-    // 8-row groups every 512 bytes.
+    // Sᵀ += 1 · (-LSE/scale parts) and dPᵀ += 1 · (-D parts) in one K = 16
+    // step over both (dPᵀ's columns follow Sᵀ's), so Pᵀ = exp2(Sᵀ·scale·
+    // log2e) and dSᵀ = Pᵀ ∘ dPᵀ need no per-column loads. Layout: core
+    // matrices of 8 rows x 16 bytes, 2 along K (lbo 128), 8-row groups every
+    // 256 bytes; A = 128 x 16 ones, B = 2·BQ rows (the -LSE parts of the BQ
+    // query rows, then their -D parts) x 16.
+    constexpr uint32_t idesc_aug = tc::idesc_bf16_f32(kBK, 2 * BQ, false, false);
+    static_assert(C::col_dp(0) == C::col_s(0) + BQ, "dPᵀ columns follow Sᵀ's");
     const uint64_t ones = tc::smem_desc(smem_u32(smem + C::kOffOnes), 128, 256, tc::kLayoutNone);
-    const uint64_t aug = tc::smem_desc(smem_u32(smem + C::kOffAug + st * C::kAugTile), 128, 512,
+    const uint64_t aug = tc::smem_desc(smem_u32(smem + C::kOffAug + st * C::kAugTile), 128, 256,
                                        tc::kLayoutNone);
-    tc::mma_ss_warp(tmem + C::col_s(b), ones, aug, idesc_sdp, 1u);
-    tc::mma_ss_warp(tmem + C::col_dp(b), ones, aug + (256 >> 4), idesc_sdp, 1u);
+    tc::mma_ss_warp(tmem + C::col_s(b), ones, aug, idesc_aug, 1u);
   }
   tc::mma_commit_warp(done);
 }
@@ -486,15 +487,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
                                                        ((s / C::kQStages) - 1) & 1, abort_flag));
       if (!ok) break;
       if (C::kAugTerms) {
-        // query row n: 8-row group n/8 at 512 bytes, row n%8 at 16 bytes;
-        // chunk 0 = three bf16 parts of -LSE/scale (exact sum), chunk 2 =
-        // three parts of -D; chunks 1 and 3 stay zero
+        // B row n (8-row group n/8 at 256 bytes, row n%8 at 16 bytes, first
+        // K chunk) = three bf16 parts of -LSE/scale of query row n (exact
+        // sum); B row BQ + n (2048 bytes further: BQ/8 groups) = three parts
+        // of its -D; the second K chunk of every row stays zero
         uint8_t* aug = smem + C::kOffAug + st * C::kAugTile;
         const float inv_c = 1.f / (scale * kLog2e);
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
           const int nrow = u * 32 + lane;
-          uint8_t* rowp = aug + (nrow >> 3) * 512 + (nrow & 7) * 16;
+          uint8_t* rowp = aug + (nrow >> 3) * 256 + (nrow & 7) * 16;
           float vals[2] = {nl[u] * inv_c, nd[u]};
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
@@ -507,7 +509,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
             const uint32_t w0 = uint32_t(__bfloat16_as_ushort(h1)) |
                                 (uint32_t(__bfloat16_as_ushort(h2)) << 16);
             const uint32_t w1 = uint32_t(__bfloat16_as_ushort(h3));
-            *reinterpret_cast<uint4*>(rowp + w * 256) = make_uint4(w0, w1, 0u, 0u);
+            *reinterpret_cast<uint4*>(rowp + w * (BQ / 8) * 256) = make_uint4(w0, w1, 0u, 0u);
           }
         }
         fence_proxy_async_smem();   // read by the tensor core (async proxy)
