@@ -187,10 +187,11 @@ ATTN_DEVINL void bwd_issue_sdp(uint8_t* smem, uint32_t tmem, int s, uint64_t* do
 // copy to shared memory for dQ. masked_row: some column may be hidden, then
 // (no general mask) columns before qmin and every column of a key past Nk
 // get P = 0, or (general mask) the columns whose row interval in keys_st
-// does not contain the key.
-template <int D, bool kGeneral>
+// does not contain the key; a window mask also hides the columns past qmax.
+template <int D, bool kGeneral, bool kWin>
 ATTN_DEVINL void bwd_pds_step(uint8_t* smem, uint32_t tmem, uint32_t lane_base, int b, int st,
-                              int r, int key, bool key_in, int cbase, int qmin, bool masked_row,
+                              int r, int key, bool key_in, int cbase, int qmin, int qmax,
+                              bool masked_row,
                               float c, const int4* keys_st) {
   using C = BwdCfg<D>;
   constexpr int BQ = C::BQ;
@@ -228,8 +229,8 @@ ATTN_DEVINL void bwd_pds_step(uint8_t* smem, uint32_t tmem, uint32_t lane_base, 
               if (!load_row_keys(&keys_st[col]).visible(key)) p.x = 0.f;
               if (!load_row_keys(&keys_st[col + 1]).visible(key)) p.y = 0.f;
             } else {
-              if (!key_in || col < qmin) p.x = 0.f;
-              if (!key_in || col + 1 < qmin) p.y = 0.f;
+              if (!key_in || col < qmin || (kWin && col > qmax)) p.x = 0.f;
+              if (!key_in || col + 1 < qmin || (kWin && col + 1 > qmax)) p.y = 0.f;
             }
           }
           const f2 dpd = add2(f2{__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])},
@@ -264,6 +265,21 @@ struct StepPlan {
     first_tile = 0;
     if (causal) first_tile = max(0, k0 - (Nk - Nq)) / BQ;
     tiles_per_head = max(0, nq_tiles - first_tile);
+    n = (k0 < Nk) ? tiles_per_head * group : 0;
+  }
+  // Keys [k0, k1] and a window mask (row i sees keys i' - wl .. i' + wr,
+  // i' = i + Nk - Nq; a negative bound is open): the rows that see one of
+  // the keys are i in [k0 - wr - shift, k1 + wl - shift], one run of tiles.
+  ATTN_DEVINL void init_window(int k0, int k1, int Nq, int Nk, int wl, int wr, int group_,
+                               int BQ) {
+    group = group_;
+    list = nullptr;
+    const long long shift = (long long)Nk - Nq;
+    long long lo = 0, hi = (long long)Nq - 1;
+    if (wr >= 0) lo = max(lo, (long long)k0 - wr - shift);
+    if (wl >= 0) hi = min(hi, (long long)k1 + wl - shift);
+    first_tile = lo <= hi ? int(lo / BQ) : 0;
+    tiles_per_head = lo <= hi ? int(hi / BQ) - first_tile + 1 : 0;
     n = (k0 < Nk) ? tiles_per_head * group : 0;
   }
   ATTN_DEVINL void init_listed(const unsigned short* list_, int count, int group_, int k0, int Nk) {
@@ -320,9 +336,10 @@ ATTN_DEVINL int list_query_tiles(const MaskSpec& m, int b, int k0, int k1, int N
   return *count;
 }
 
-// kGeneral = false: no mask or causal only; true: any MaskSpec (listed query
-// tiles, per-step row key intervals, per-element masking of straddling steps).
-template <int D, bool kGeneral>
+// kGeneral = false: no mask, causal, or a window (query tiles and masked
+// columns from the window's bounds); true: any MaskSpec (listed query tiles,
+// per-step row key intervals, per-element masking of straddling steps).
+template <int D, bool kGeneral, bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
               const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -355,7 +372,11 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   const int group = Hq / Hkv;
   const int k0 = ktile * kBK;
   StepPlan plan;
-  if (!kGeneral) plan.init(k0, Nq, Nk, mask.window_right == 0, group, BQ);
+  if (kWin)
+    plan.init_window(k0, min(k0 + kBK - 1, Nk - 1), Nq, Nk, mask.window_left, mask.window_right,
+                     group, BQ);
+  else if (!kGeneral)
+    plan.init(k0, Nq, Nk, mask.window_right == 0, group, BQ);
 
   if (tid == 0) {
     bars.abort = 0;
@@ -665,12 +686,24 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc::fence_after_sync();
       const bool key_in = key < Nk;
-      // first visible query column of this key row (causal), relative to q0;
-      // general masks: the step is masked unless every pair is visible
-      const int qmin = (!kGeneral && mask.window_right == 0) ? key - shift - q0 : -1;
-      const bool masked_row = kGeneral ? stage_clean[st] == 0 : (!key_in || qmin > cbase);
-      bwd_pds_step<D, kGeneral>(smem, tmem, lane_base, b, st, r, key, key_in, cbase, qmin,
-                                masked_row, c, kGeneral ? &stage_keys[st][0] : nullptr);
+      // first and last query columns (relative to q0) that see this key row
+      // under a window mask (causal: the first only); general masks: the
+      // step is masked unless every pair is visible
+      int qmin = (!kGeneral && mask.window_right == 0) ? key - shift - q0 : -1;
+      int qmax = INT_MAX;
+      if (kWin) {
+        qmin = mask.window_right >= 0
+                   ? int(clampll((long long)key - mask.window_right - shift - q0, INT_MIN, INT_MAX))
+                   : INT_MIN;
+        qmax = mask.window_left >= 0
+                   ? int(clampll((long long)key + mask.window_left - shift - q0, INT_MIN, INT_MAX))
+                   : INT_MAX;
+      }
+      const bool masked_row = kGeneral ? stage_clean[st] == 0
+                              : (!key_in || qmin > cbase || (kWin && qmax < cbase + CW - 1));
+      bwd_pds_step<D, kGeneral, kWin>(smem, tmem, lane_base, b, st, r, key, key_in, cbase, qmin,
+                                      qmax, masked_row, c,
+                                      kGeneral ? &stage_keys[st][0] : nullptr);
       tc::tmem_st_wait();
       // generic-proxy writes of the dSᵀ copy -> tensor-core (async proxy) reads
       if (C::kFusedDq) fence_proxy_async_smem();
@@ -778,7 +811,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
   }
 }
 
-template <int D, bool kGeneral>
+template <int D, bool kGeneral, bool kWin>
 cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   using C = BwdCfg<D>;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
@@ -790,7 +823,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
       !make_map_bf16_3d(&mdk, a.dk, D, a.Nk, bhk, kBK) ||
       !make_map_bf16_3d(&mdv, a.dv, D, a.Nk, bhk, kBK))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D, kGeneral>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D, kGeneral, kWin>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
   if (e != cudaSuccess) return e;
   const int n_ktiles = (a.Nk + kBK - 1) / kBK;
@@ -802,7 +835,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   if (blocks > 0x7fffffffL) return cudaErrorInvalidValue;
   if (C::kFusedDq) {
     // d = 64 adds into the accumulator the preprocess zeroes: plain launch
-    bwd_tc_kernel<D, kGeneral><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
+    bwd_tc_kernel<D, kGeneral, kWin><<<unsigned(blocks), kThreads, C::kDynSmem, a.stream>>>(
         mq, mk, mv, mdo, mdk, mdv, a.lse, a.row_term, a.dq_acc, a.Hq, a.Hkv, a.Nq, a.Nk,
         a.scale, a.mask, n_ktiles, order_grp);
     return cudaGetLastError();
@@ -820,7 +853,7 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, kGeneral>, mq, mk, mv, mdo, mdk, mdv, a.lse,
+  return cudaLaunchKernelEx(&cfg, bwd_tc_kernel<D, kGeneral, kWin>, mq, mk, mv, mdo, mdk, mdv, a.lse,
                             static_cast<const float*>(a.row_term), a.dq_acc, a.Hq, a.Hkv, a.Nq,
                             a.Nk, a.scale, a.mask, n_ktiles, order_grp);
 }
@@ -829,10 +862,16 @@ cudaError_t launch_bwd_tc_d(const BwdArgs& a) {
 
 cudaError_t launch_bwd_tc(const BwdArgs& a) {
   const MaskSpec& m = a.mask;
-  const bool plain = m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
-                     m.row_kv_start == nullptr;   // no mask, or causal
-  if (plain) return a.d == 64 ? launch_bwd_tc_d<64, false>(a) : launch_bwd_tc_d<128, false>(a);
-  return a.d == 64 ? launch_bwd_tc_d<64, true>(a) : launch_bwd_tc_d<128, true>(a);
+  // no mask or causal; a window (query tiles and masks from its bounds);
+  // anything else through the listed query tiles and row intervals
+  const bool causal_only = m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
+                           m.row_kv_start == nullptr;
+  const bool window = m.n_global == 0 && m.row_kv_start == nullptr;
+  if (causal_only)
+    return a.d == 64 ? launch_bwd_tc_d<64, false, false>(a) : launch_bwd_tc_d<128, false, false>(a);
+  if (window)
+    return a.d == 64 ? launch_bwd_tc_d<64, false, true>(a) : launch_bwd_tc_d<128, false, true>(a);
+  return a.d == 64 ? launch_bwd_tc_d<64, true, false>(a) : launch_bwd_tc_d<128, true, false>(a);
 }
 
 }  // namespace attn
