@@ -190,9 +190,10 @@ ATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const
  * attn_bwd under a general mask (see attn_mask; mask == NULL: no mask): the
  * same mask the forward used, so P is zero on every hidden (row, key) pair
  * and on rows that see no key (LSE = -inf). Any Nq, Nk > 0; with dt =
- * ATTN_BF16 and a mask other than none or causal, Nq is limited to 65536
- * (d = 128) or 131072 (d = 64): ATTN_ERR_UNSUPPORTED beyond. Otherwise as
- * attn_bwd, with the same workspace.
+ * ATTN_BF16 and a mask with global keys or per-row key ranges, Nq is
+ * limited to 65536 (d = 128) or 131072 (d = 64): ATTN_ERR_UNSUPPORTED
+ * beyond (windows alone have no limit). Otherwise as attn_bwd, with the
+ * same workspace.
  */
 ATTN_API attn_status attn_bwd_masked(const void* q, const void* k, const void* v, const void* o,
                                      const void* dO, const float* lse, void* dq, void* dk,

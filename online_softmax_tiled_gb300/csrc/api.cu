@@ -181,9 +181,11 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_MISALIGNED;
   const bool plain = ms.window_left < 0 && ms.window_right <= 0 && ms.n_global == 0 &&
                      ms.row_kv_start == nullptr;
-  // general masks on the tensor-core key-tile pass list at most 1024 query
-  // tiles (64 rows at d = 128, 128 rows at d = 64) per key tile
-  if (!plain && dt == ATTN_BF16 && (Nq + (d == 128 ? 64 : 128) - 1) / (d == 128 ? 64 : 128) > 1024)
+  // masks with global keys or row ranges on the tensor-core key-tile pass
+  // list at most 1024 query tiles (64 rows at d = 128, 128 rows at d = 64)
+  // per key tile (windows take their tiles from the bounds)
+  const bool listed = ms.n_global != 0 || ms.row_kv_start != nullptr;
+  if (listed && dt == ATTN_BF16 && (Nq + (d == 128 ? 64 : 128) - 1) / (d == 128 ? 64 : 128) > 1024)
     return ATTN_ERR_UNSUPPORTED;
   const int causal = (plain && ms.window_right == 0) ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
@@ -191,7 +193,7 @@ attn_status bwd_common(const void* q, const void* k, const void* v, const void* 
             reinterpret_cast<float*>(ws + lay.row_term), reinterpret_cast<float*>(ws + lay.dq_acc),
             static_cast<cudaStream_t>(stream), true};
   a.mask = ms;
-  if (bwd_persistent(d, dt, ms)) a.sched = reinterpret_cast<int*>(ws + lay.sched);
+  if (bwd_persistent(d, dt, ms, Nq, Nk)) a.sched = reinterpret_cast<int*>(ws + lay.sched);
   // bf16, d = 128: a key-tile pass (dK, dV) and a query-tile pass (dQ, written
   // in bf16 directly; the float32 accumulator is not used). Otherwise one
   // pass adds dQ into the float32 accumulator, converted at the end.

@@ -127,13 +127,14 @@ ATTN_DEVINL void mma_dsk(uint32_t d_tmem, uint32_t s_tmem, uint32_t ka, bool fir
 // dS = P ∘ (dP - D) over one thread's 64 key columns of a step, as bf16
 // pairs: P = exp2(S·scale·log2e - LSE·log2e) (c = scale·log2e, nl =
 // -LSE·log2e, nd = -D), zero on keys the row does not see. Without a
-// general mask (kGeneral = false) those are the keys past `limit`; with one,
+// general mask (kGeneral = false) those are the keys past `limit` (and, with
+// kLo, before `lo`: a window's left edge); with one,
 // the clear bits of the 32-bit visibility masks vis0 (first 32 columns) and
 // vis1. `masked` = false: every column is visible.
-template <bool kGeneral>
+template <bool kGeneral, bool kLo = false>
 ATTN_DEVINL void ds_pairs(const uint32_t (&sr)[64], const uint32_t (&dr)[64], float c, float nl,
                           float nd, bool masked, int key0, int limit, uint32_t vis0,
-                          uint32_t vis1, uint32_t (&pk)[32]) {
+                          uint32_t vis1, uint32_t (&pk)[32], int lo = 0) {
   const f2 c2{c, c}, nl2{nl, nl}, nd2{nd, nd};
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
@@ -145,8 +146,8 @@ ATTN_DEVINL void ds_pairs(const uint32_t (&sr)[64], const uint32_t (&dr)[64], fl
         if (!(vis & (1u << ((2 * e) & 31)))) p.x = 0.f;
         if (!(vis & (1u << ((2 * e + 1) & 31)))) p.y = 0.f;
       } else {
-        if (key0 + 2 * e > limit) p.x = 0.f;
-        if (key0 + 2 * e + 1 > limit) p.y = 0.f;
+        if (key0 + 2 * e > limit || (kLo && key0 + 2 * e < lo)) p.x = 0.f;
+        if (key0 + 2 * e + 1 > limit || (kLo && key0 + 2 * e + 1 < lo)) p.y = 0.f;
       }
     }
     const f2 dpd = add2(f2{__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])}, nd2);
@@ -507,6 +508,7 @@ ATTN_DEVINL void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int 
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2) : "memory");
 }
 
+template <bool kWin>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
@@ -514,8 +516,8 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_do,
                          __nv_bfloat16* __restrict__ dq, const float* __restrict__ lse,
                          const float* __restrict__ row_term, int* __restrict__ counter, int Hq,
-                         int Hkv, int Nq, int Nk, float scale, int causal, int n_qt, int n_items,
-                         int order_grp) {
+                         int Hkv, int Nq, int Nk, float scale, int causal, int win_left,
+                         int win_right, int n_qt, int n_items, int order_grp) {
   using C = DqCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -570,7 +572,24 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
     if (lane == 0 && ok) mbar_arrive(&bars.item_empty[slot]);
     return w;
   };
-  auto steps_of = [&](int qt) { return key_tiles_for(qt * kBM, Nq, Nk, causal); };
+  // Key tiles first .. first + n - 1 of query tile qt: from 0 (no mask,
+  // causal), or (window: row i sees keys i' - win_left .. i' + win_right,
+  // i' = i + Nk - Nq, a negative bound open) the tiles of the keys its rows
+  // see; the launch guarantees at least one.
+  auto tiles_of = [&](int qt, int& first) -> int {
+    first = 0;
+    if (!kWin) return key_tiles_for(qt * kBM, Nq, Nk, causal);
+    const int q0 = qt * kBM;
+    if (q0 >= Nq) return 0;
+    const long long shift = (long long)Nk - Nq;
+    const long long q1 = min(q0 + kBM - 1, Nq - 1);
+    const long long lo = win_left >= 0 ? max(0LL, q0 + shift - win_left) : 0LL;
+    const long long hi =
+        win_right >= 0 ? min((long long)Nk - 1, q1 + shift + win_right) : (long long)Nk - 1;
+    if (lo > hi) return 0;
+    first = int(lo / kBN);
+    return int(hi / kBN) - first + 1;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler, Q / dO producer
@@ -647,7 +666,8 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
         int bh, qt;
         dq_item(w, n_qt, n_heads, order_grp, bh, qt);
         const int kvh = (bh / Hq) * Hkv + (bh % Hq) / (Hq / Hkv);
-        const int n = steps_of(qt);
+        int first;
+        const int n = tiles_of(qt, first);
         for (int j = 0; j < n && ok; ++j, ++g) {
           const int sk = g % kKStages, sv = g % kVStages;
           if (g >= kKStages) ok = mbar_wait_bounded(&bars.k_empty[sk], ((g / kKStages) - 1) & 1, abort_flag);
@@ -655,14 +675,14 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
           mbar_arrive_expect_tx(&bars.k_full[sk], C::kTile);
           for (int a = 0; a < kD / 64; ++a)
             tc::tma_load_3d(smem + C::kOffK + sk * C::kTile + a * (kBN * 128), &map_k, 64 * a,
-                            j * kBN, kvh, &bars.k_full[sk]);
+                            (first + j) * kBN, kvh, &bars.k_full[sk]);
           ++issued_k;
           if (g >= kVStages) ok = mbar_wait_bounded(&bars.v_empty[sv], ((g / kVStages) - 1) & 1, abort_flag);
           if (!ok) break;
           mbar_arrive_expect_tx(&bars.v_full[sv], C::kTile);
           for (int a = 0; a < kD / 64; ++a)
             tc::tma_load_3d(smem + C::kOffV + sv * C::kTile + a * (kBN * 128), &map_v, 64 * a,
-                            j * kBN, kvh, &bars.v_full[sv]);
+                            (first + j) * kBN, kvh, &bars.v_full[sv]);
           ++issued_v;
         }
       }
@@ -705,7 +725,8 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
       if (!ok || w < 0) break;
       int bh, qt;
       dq_item(w, n_qt, n_heads, order_grp, bh, qt);
-      const int n = steps_of(qt);
+      int first;
+      const int n = tiles_of(qt, first);
       // Item start: S and dP of its first step, S of its second. The tensor
       // pipe runs this warp's MMAs in order: S(g0) overwrites the S buffer
       // only after the previous item's dQ has read dS from it, dP(g0) the dP
@@ -776,7 +797,8 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
       if (!ok || w < 0) break;
       int bh, qt;
       dq_item(w, n_qt, n_heads, order_grp, bh, qt);
-      const int n = steps_of(qt);
+      int first;
+      const int n = tiles_of(qt, first);
       const int row = qt * kBM + r;
       const bool row_in = row < Nq;
       const size_t ri = size_t(bh) * Nq + (row_in ? row : 0);
@@ -784,7 +806,14 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
       const float lse_r = row_in ? lse[ri] : -INFINITY;
       const float nl = lse_r == -INFINITY ? -INFINITY : -lse_r * kLog2e;   // -LSE·log2e
       const float nd = row_in ? -row_term[ri] : 0.f;                       // -D
-      const int limit = causal ? min(Nk - 1, row + (Nk - Nq)) : Nk - 1;
+      // keys this row sees: lo .. limit
+      int limit = causal ? min(Nk - 1, row + (Nk - Nq)) : Nk - 1;
+      int lo = 0;
+      if (kWin) {
+        const long long ip = (long long)row + Nk - Nq;
+        limit = win_right >= 0 ? int(min((long long)Nk - 1, ip + win_right)) : Nk - 1;
+        lo = win_left >= 0 ? int(max(0LL, min((long long)Nk, ip - win_left))) : 0;
+      }
       for (int j = 0; j < n; ++j, ++g) {
         if (!mbar_wait2_warp(&bars.s_full[g & 1], (g >> 1) & 1, &bars.dp_full, g & 1,
                              abort_flag)) {
@@ -803,9 +832,10 @@ bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
         tc::tmem_ld_wait();
         tc::fence_before_sync();
         mbar_arrive(&bars.dp_free);                  // dP(g+1) may overwrite dP now
-        const int key0 = j * kBN + half * 64;
+        const int key0 = (first + j) * kBN + half * 64;
         uint32_t pk[32];                             // dS as bf16 pairs
-        ds_pairs<false>(sr, dr, c, nl, nd, key0 + 63 > limit, key0, limit, 0u, 0u, pk);
+        ds_pairs<false, kWin>(sr, dr, c, nl, nd, key0 + 63 > limit || (kWin && key0 < lo), key0,
+                              limit, 0u, 0u, pk, lo);
         tmem_st32(s_addr, pk);                       // over the S columns just read
         tc::tmem_st_wait();
         tc::fence_before_sync();
@@ -869,12 +899,14 @@ cudaError_t launch_bwd_dq(const BwdArgs& a) {
   const long items = long(n_qt) * a.B * a.Hq;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int order_grp = order_group(m.varies(), 4LL * a.Nk * kD);
-  if (a.sched != nullptr && bwd_persistent(a.d, a.dt, m)) {
+  if (a.sched != nullptr && bwd_persistent(a.d, a.dt, m, a.Nq, a.Nk)) {
     // one CTA per SM, work from the counter; a programmatic dependent of the
     // key-tile pass, which lets it start once the preprocess (row term,
     // counter) is complete
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_persistent_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynSmem);
+    const bool win = bwd_dq_window(m);
+    const auto kern = win ? bwd_dq_persistent_kernel<true> : bwd_dq_persistent_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kDynSmem);
     if (e != cudaSuccess) return e;
     const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidValue;
@@ -888,10 +920,10 @@ cudaError_t launch_bwd_dq(const BwdArgs& a) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bwd_dq_persistent_kernel, mq, mk, mv, mdo,
-                              static_cast<__nv_bfloat16*>(a.dq), a.lse,
-                              static_cast<const float*>(a.row_term), a.sched, a.Hq, a.Hkv,
-                              a.Nq, a.Nk, a.scale, a.causal, n_qt, int(items), order_grp);
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, static_cast<__nv_bfloat16*>(a.dq),
+                              a.lse, static_cast<const float*>(a.row_term), a.sched, a.Hq, a.Hkv,
+                              a.Nq, a.Nk, a.scale, a.causal, m.window_left, m.window_right, n_qt,
+                              int(items), order_grp);
   }
   const bool general = !(m.window_left < 0 && m.window_right <= 0 && m.n_global == 0 &&
                          m.row_kv_start == nullptr);

@@ -183,11 +183,18 @@ inline int order_group(bool causal, long long bytes_per_head, long long budget =
 // Workspace carving (bytes, 256-aligned sections).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// The bf16 d = 128 backward without a general mask runs its dQ pass as a
-// persistent grid that takes work from a counter in the workspace.
-inline bool bwd_persistent(int d, attn_dtype dt, const MaskSpec& m) {
-  return dt == ATTN_BF16 && d == 128 && m.window_left < 0 && m.window_right <= 0 &&
-         m.n_global == 0 && m.row_kv_start == nullptr;
+// The bf16 d = 128 backward runs its dQ pass as a persistent grid that takes
+// work from a counter in the workspace, with no mask, causal, or a window
+// under which every query tile sees a key (always so for Nq <= Nk or a
+// window open to the right); other masks use one CTA per query tile.
+inline bool bwd_persistent(int d, attn_dtype dt, const MaskSpec& m, int Nq, int Nk) {
+  if (dt != ATTN_BF16 || d != 128 || m.n_global != 0 || m.row_kv_start != nullptr) return false;
+  const bool causal_only = m.window_left < 0 && m.window_right <= 0;
+  return causal_only || Nq <= Nk || m.window_right < 0;
+}
+// (the persistent dQ pass's window form: any window but plain causal)
+inline bool bwd_dq_window(const MaskSpec& m) {
+  return !(m.window_left < 0 && m.window_right <= 0);
 }
 
 cudaError_t launch_fwd_simt(const FwdArgs& a);

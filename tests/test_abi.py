@@ -211,9 +211,10 @@ def test_bwd_masked_rejects_before_launch(lib):
     assert call(AttnMask(-1, 0, 0, P, P + 1)) == MISALIGNED
     assert call(AttnMask(7, 0, 0, None, None), ws_bytes=need - 1) == WORKSPACE
     assert call(AttnMask(7, 0, 0, None, None), scale=-1.0) == INVALID
-    # a general bf16 mask lists at most 1024 query tiles per key tile
+    # a bf16 mask with global keys (or row ranges) lists at most 1024 query
+    # tiles per key tile; a window alone takes its tiles from its bounds
     big = lib.attn_bwd_workspace_size(1, 2, 2, 70000, 16, 128)
-    assert call(AttnMask(7, 0, 0, None, None), Nq=70000, d=128, ws_bytes=big) == UNSUPPORTED
+    assert call(AttnMask(7, 0, 4, None, None), Nq=70000, d=128, ws_bytes=big) == UNSUPPORTED
 
 
 def test_decode_sparse_rejects_before_launch(lib):

@@ -192,11 +192,13 @@ def test_backward_empty_rows_and_unequal_lengths(ost, dtype, d):
 
 @pytest.mark.parametrize("dtype,d", BWD_DT)
 @pytest.mark.parametrize("nq,nk,wl,wr", [(900, 1300, 300, 50), (2100, 2100, 1023, 0),
-                                         (1000, 1000, 0, 200)])
+                                         (1000, 1000, 0, 200), (1300, 900, 300, 50),
+                                         (1100, 700, 200, -1)])
 def test_backward_windows_over_many_tiles(ost, dtype, d, nq, nk, wl, wr):
     """Sliding windows whose key range spans several key tiles and query
-    steps: both bounds cut through steps, Nq < Nk shifts the window, and a
-    window reaching only right of the diagonal."""
+    steps: both bounds cut through steps, Nq < Nk shifts the window, a
+    window reaching only right of the diagonal, Nq > Nk with early rows that
+    see no key, and a window open to the right."""
     if dtype == "f32" and wl >= 1000:
         # float32 sums over ~1000 visible queries per key reach ~1e-5 at
         # |dV| ~ 6, the size of the absolute bound itself; the float32
