@@ -470,7 +470,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__
 }
 
 // ----------------------------------------------------------------------------
-// Persistent form (no mask, or causal): one CTA per SM takes 128-row query
+// Persistent form (no mask, causal, or a window): one CTA per SM takes 128-row query
 // tiles in turn, the first from its CTA index and the others from a device
 // counter (dynamic scheduling: a CTA that finishes early takes the next
 // tile, so the causal mix of long and short tiles balances). Tiles are
