@@ -87,6 +87,30 @@ def test_merge_kernel_permuted_and_empty_splits(ost, out_dtype):
     assert np.max(np.abs(got_lse[fin] - lse_ref[fin])) <= 1e-5
 
 
+@pytest.mark.parametrize("d,S", [(4, 1), (96, 3), (256, 33)])
+def test_merge_kernel_any_width(ost, d, S):
+    """The merge on its own for any row width that is a multiple of 4 up to
+    256 and split counts from 1 to more than a warp, with random partials
+    (maxima spread over 40 units, some splits empty) against the oracle."""
+    rng = np.random.default_rng(d + S)
+    rows = 37
+    m_p = rng.uniform(-20.0, 20.0, (rows, S))
+    m_p[rng.random((rows, S)) < 0.2] = -np.inf
+    l_p = np.where(np.isneginf(m_p), 0.0, rng.uniform(0.5, 50.0, (rows, S)))
+    o_p = np.where(np.isneginf(m_p)[..., None], 0.0, rng.standard_normal((rows, S, d)) * 3.0)
+    o_ref, lse_ref = oracle.merge_partials(o_p, m_p, l_p)
+    t = lambda a: torch.tensor(a, dtype=torch.float32, device=DEV).contiguous()
+    o = torch.empty((rows, d), dtype=torch.float32, device=DEV)
+    lse = torch.empty(rows, dtype=torch.float32, device=DEV)
+    ost.attn_merge_partials(t(o_p), t(m_p), t(l_p), o, lse)
+    torch.cuda.synchronize()
+    got, got_lse = to_f64(o), to_f64(lse)
+    empty = np.isneginf(lse_ref)
+    assert np.all(np.isneginf(got_lse[empty])) and np.all(got[empty] == 0)
+    assert np.max(np.abs(got[~empty] - o_ref[~empty]), initial=0.0) <= 1e-5 * np.max(np.abs(o_ref))
+    assert np.max(np.abs(got_lse[~empty] - lse_ref[~empty]), initial=0.0) <= 1e-5 * 25
+
+
 def test_long_cache(ost):
     """One request with a 131072-key cache, 64 splits of 2048 keys, GQA 4:1,
     and a cache whose length is not a multiple of the split count."""
